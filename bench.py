@@ -1,0 +1,425 @@
+#!/usr/bin/env python
+"""Benchmark of the fused LongFlow decode step (attention + LongFlowScore +
+eviction) on GB300.
+
+Default workload: the Qwen3-8B Fig. 1 shape of "LongFlow: Efficient KV Cache
+Compression for Reasoning Models" (batch 128, 32 query / 8 KV heads, head dim
+128, 3200 cache slots, W = 32), with synthetic seeded bf16 data.
+
+A step is one call of lf_decode_step over the whole batch: slot write, mask
+ageing, attention, score and argmin for every (b, kvh) unit. The step's
+write_slot is the previous step's next_slot (every-step eviction), kept on the
+device. Inputs are resident in HBM before timing starts; the K/V caches
+(1.68 GB) are far larger than the 129 MB L2, so no flush is needed.
+
+Output: one JSON line on rank 0 (see the keys at the end of main()).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+Under torchrun each rank runs its own batch of sequences (weak scaling, no
+collective on the data path); the time reported is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from decode_kv_cache_step_gb300.workloads import (  # noqa: E402
+    WORKLOADS, algorithmic_bytes, initial_state, live_lengths, sequence_state, step_inputs)
+
+METRIC = "decode steps/s and achieved HBM GB/s (% of GB300 peak) for fused attn+score+evict"
+DEFAULT_WORKLOAD = "qwen3_8b_b128_s3200"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "lf_attn_split_kernel.qwen3_8b_b128_s3200.md")
+SPLIT_SOURCES = ["lf_attn_split.cu", "lf_ptx.cuh", "lf_kernels.h"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in SPLIT_SOURCES:
+        with open(os.path.join(ROOT, "decode_kv_cache_step_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """dram read+write bytes per launch of the split kernel from the committed ncu
+    summary, or None if absent or taken on another version of the kernel."""
+    try:
+        with open(PROFILE_SUMMARY) as fh:
+            text = fh.read()
+    except OSError:
+        return None
+    src, traffic = None, None
+    for line in text.splitlines():
+        if line.startswith("source_sha:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith("traffic_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    if src != kernel_source_hash():
+        return None
+    return traffic
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return json.load(fh), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed work runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(period_ms), "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((time.monotonic(), parts))
+
+    def mark(self):
+        return time.monotonic()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = [r for t, r in self.rows if t0 - 0.06 <= t <= t1 + 0.06] or [r for _, r in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def bf16_dev(a, device):
+    import torch
+    return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def run_oracle_steps(wl, state, max_seconds: float, max_steps: int, units=None):
+    """Times oracle steps (the CPU baseline); returns (steps, seconds, threads)."""
+    import oracle
+    ws = np.full((wl.B, wl.Hkv), -1, dtype=np.int32)
+    done, t_total = 0, 0.0
+    while done < max_steps and (t_total < max_seconds or done == 0):
+        inp = step_inputs(wl, 1000 + done)
+        t0 = time.perf_counter()
+        res = oracle.decode_step(inp["q"], state["k_cache"], state["v_cache"], state["mask"],
+                                 inp["new_k"], inp["new_v"], ws, wl.W, wl.scale, units=units)
+        t_total += time.perf_counter() - t0
+        ws = res["next_slot"].copy()
+        if units is not None:
+            ws[ws < -1] = -1
+        done += 1
+    return done, t_total, oracle.max_threads()
+
+
+def bench_reference(args, wl):
+    """The fp64 CPU oracle on the host cores, on a bounded sample of units per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    sample_units = min(wl.units, max(1, args.reference_units))
+    rng = np.random.default_rng(0)
+    units = np.sort(rng.choice(wl.units, size=sample_units, replace=False)).astype(np.int32)
+    seqs = sorted({int(u) // wl.Hkv for u in units})
+    # Host state with only the sampled sequences filled (the oracle touches only them).
+    k = np.zeros((wl.B, wl.Hkv, wl.S, wl.d), dtype=np.uint16)
+    v = np.zeros_like(k)
+    mask = np.full((wl.B, wl.Hkv, wl.S), -1, dtype=np.int32)
+    for b in seqs:
+        k[b], v[b], mask[b], _ = sequence_state(wl, b)
+    state = {"k_cache": k, "v_cache": v, "mask": mask}
+    ws = np.full((wl.B, wl.Hkv), -1, dtype=np.int32)
+
+    def one(step):
+        nonlocal ws
+        inp = step_inputs(wl, step)
+        res = oracle.decode_step(inp["q"], k, v, mask, inp["new_k"], inp["new_v"], ws, wl.W,
+                                 wl.scale, units=units)
+        nxt = res["next_slot"].copy()
+        nxt[nxt < -1] = -1
+        ws = nxt
+
+    for s in range(args.warmup):
+        one(s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        one(args.warmup + s)
+    dt = time.perf_counter() - t0
+    scale_to_full = wl.units / sample_units
+    sec_per_step = dt / args.steps * scale_to_full
+    value = 1.0 / sec_per_step
+    cores = oracle.max_threads()
+    sample = (f"{sample_units} of {wl.units} (b,kvh) units per step, scaled by "
+              f"{scale_to_full:.1f} to a full step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl, world),
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl, world):
+    return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d, "S": wl.S,
+            "W": wl.W, "live": list(wl.live) if isinstance(wl.live, tuple) else wl.live,
+            "description": wl.description,
+            "l2": "inputs larger than L2 (K/V caches >> 129 MB); no flush between steps",
+            "parallelism": f"replicas x{world} (disjoint sequences, no collective)"}
+
+
+def bench_lf(args, wl):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    import decode_kv_cache_step_gb300 as lf
+    from decode_kv_cache_step_gb300 import build as lfbuild
+    if not lfbuild.up_to_date() and rank == 0:
+        lfbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    lf.load_library()
+
+    # Each rank runs its own B sequences of the recipe (weak scaling).
+    host = initial_state(wl, batch_offset=rank * wl.B)
+    lengths = host["lengths"]
+    k = bf16_dev(host["k_cache"], device)
+    v = bf16_dev(host["v_cache"], device)
+    mask = torch.from_numpy(host["mask"]).to(device)
+    pool = []
+    for s in range(8):
+        inp = step_inputs(wl, s, batch_offset=rank * wl.B, full_batch=wl.B * world)
+        pool.append({kk: bf16_dev(vv, device) for kk, vv in inp.items()})
+    out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.bfloat16, device=device)
+    slots = [torch.full((wl.B, wl.Hkv), -1, dtype=torch.int32, device=device),
+             torch.empty((wl.B, wl.Hkv), dtype=torch.int32, device=device)]
+    stream = torch.cuda.current_stream(device)
+
+    def step(i):
+        p = pool[i % len(pool)]
+        lf.decode_step(p["q"], k, v, mask, p["new_k"], p["new_v"], slots[i % 2], out,
+                       slots[(i + 1) % 2], wl.W, wl.scale, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if lf.device_errors(stream) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # ---------------------------------------------------------- device-timed
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    lf.profile_collect(lf.LF_KERNEL_ATTN_SPLIT)
+    lf.profile_collect(lf.LF_KERNEL_COMBINE)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    lf.profile_enable(True)
+    t_wall0 = clocks.mark()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = clocks.mark()
+    lf.profile_enable(False)
+    ms_total = ev0.elapsed_time(ev1)
+    split_ms, split_n = lf.profile_collect(lf.LF_KERNEL_ATTN_SPLIT)
+    comb_ms, comb_n = lf.profile_collect(lf.LF_KERNEL_COMBINE)
+    if world > 1:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    if lf.device_errors(stream) != 0:
+        raise RuntimeError("device error word set during the timed steps")
+
+    # ------------------------------------------------------ end to end (host)
+    pin = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+    hpool = []
+    for s in range(8):
+        inp = step_inputs(wl, s, batch_offset=rank * wl.B, full_batch=wl.B * world)
+        hpool.append({kk: pin(vv).view(torch.bfloat16) for kk, vv in inp.items()})
+    h_out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.bfloat16).pin_memory()
+    h_ws = torch.full((wl.B, wl.Hkv), -1, dtype=torch.int32).pin_memory()
+    h_next = torch.empty((wl.B, wl.Hkv), dtype=torch.int32).pin_memory()
+
+    def e2e_step(i):
+        p = hpool[i % len(hpool)]
+        lf.decode_step_host(p["q"], k, v, mask, p["new_k"], p["new_v"], h_ws, h_out, h_next,
+                            wl.W, wl.scale, stream=stream)
+        stream.synchronize()
+        h_ws.copy_(h_next)
+
+    for i in range(min(args.warmup, 5)):
+        e2e_step(i)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i)
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    clocks.stop()
+    h2d = (wl.B * wl.Hq * wl.d * 2) + 2 * (wl.B * wl.Hkv * wl.d * 2) + wl.B * wl.Hkv * 4
+    d2h = wl.B * wl.Hq * wl.d * 2 + wl.B * wl.Hkv * 4
+
+    # ------------------------------------------------------------ CPU oracle
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        n, secs, threads = run_oracle_steps(wl, host, max_seconds=args.cpu_seconds, max_steps=50)
+        cpu = {"value": n / secs, "unit": "steps/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} full decode step(s) of the same workload, fp64, "
+                         f"{threads} OpenMP threads"}
+
+    if rank != 0:
+        return 0
+
+    ms_per_step = ms_total / args.steps
+    value = world * args.steps / (ms_total / 1e3)
+    alg = algorithmic_bytes(wl, lengths)
+    out_bytes = wl.B * wl.Hq * wl.d * 2
+    split_alg = alg - out_bytes          # the split kernel writes no output rows
+    split_avg_ms = split_ms / max(split_n, 1)
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    achieved = split_alg / (split_avg_ms / 1e3) / 1e9
+    step_gbs = alg / (ms_per_step / 1e3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": workload_config(wl, world),
+        "hbm": {"algorithmic_bytes_per_step": alg, "achieved_gbs": step_gbs,
+                "frac_of_measured_peak": step_gbs / peak, "frac_of_8000_gbs": step_gbs / 8000.0,
+                "peak_kind": peak_kind},
+        "roofline": {"kernel": "lf_attn_split_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": committed_traffic(), "algorithmic_bytes_per_launch": split_alg,
+                     "avg_launch_ms": split_avg_ms, "launches": split_n,
+                     "combine_avg_ms": comb_ms / max(comb_n, 1),
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * args.steps / e2e_s, "unit": "steps/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "lf_decode_step_host from pinned host buffers; stream sync every step"},
+        "gpu_launches": split_n + comb_n,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="lf", choices=["lf", "reference"])
+    ap.add_argument("--reference-units", type=int, default=64,
+                    help="(b,kvh) units the reference arm runs per step")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps, always
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return bench_reference(args, wl)
+    return bench_lf(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,504 @@
+// C-ABI entry points of the LongFlow decode-step library: argument checks,
+// split planning, scratch management, TMA descriptors and launches.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "../../include/lf_decode.h"
+#include "lf_kernels.h"
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int kMaxNChunk = 1024;
+constexpr int kMaxS = 1 << 20;
+
+thread_local char g_last_error[512] = "";
+
+lf_status fail(lf_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+lf_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(LF_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ----------------------------------------------------------------- scratch --
+
+struct Scratch {
+    void* base = nullptr;
+    size_t bytes = 0;
+    uint32_t* dev_err = nullptr;  // never moves once created
+};
+
+std::mutex g_mu;
+std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
+
+lf_status get_scratch(int dev, cudaStream_t stream, size_t need, Scratch** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    Scratch& s = g_scratch[{dev, stream}];
+    if (!s.dev_err) {
+        cudaError_t e = cudaMalloc(&s.dev_err, 256);
+        if (e != cudaSuccess) return fail(LF_ERR_NO_MEMORY, "cudaMalloc(error word): %s", cudaGetErrorString(e));
+        e = cudaMemset(s.dev_err, 0, 256);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+    }
+    if (s.bytes < need) {
+        if (s.base) {
+            // Work already queued on this stream may still use the old buffer.
+            cudaError_t e = cudaStreamSynchronize(stream);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+            cudaFree(s.base);
+            s.base = nullptr;
+            s.bytes = 0;
+        }
+        const size_t grow = align_up(need + need / 8, size_t(1) << 21);
+        cudaError_t e = cudaMalloc(&s.base, grow);
+        if (e != cudaSuccess) {
+            s.base = nullptr;
+            return fail(LF_ERR_NO_MEMORY, "cudaMalloc(%zu bytes of scratch): %s", grow, cudaGetErrorString(e));
+        }
+        s.bytes = grow;
+    }
+    *out = &s;
+    return LF_OK;
+}
+
+// ----------------------------------------------------------------- profile --
+
+struct ProfRec {
+    int kernel;
+    cudaEvent_t start, stop;
+};
+
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+struct ProfScope {
+    int kernel;
+    cudaStream_t stream;
+    cudaEvent_t start = nullptr, stop = nullptr;
+    ProfScope(int k, cudaStream_t s) : kernel(k), stream(s) {
+        std::lock_guard<std::mutex> lock(g_prof_mu);
+        if (!g_prof_on) return;
+        start = take_event();
+        stop = take_event();
+        if (start) cudaEventRecord(start, stream);
+    }
+    ~ProfScope() {
+        if (!start || !stop) return;
+        cudaEventRecord(stop, stream);
+        std::lock_guard<std::mutex> lock(g_prof_mu);
+        g_prof.push_back({kernel, start, stop});
+    }
+};
+
+// ------------------------------------------------------------- device info --
+
+int sm_count(int dev) {
+    static std::mutex mu;
+    static std::map<int, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    cache[dev] = n;
+    return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [units][S][D] bf16 as a 3-D tensor map, 64 x 64 x 1 boxes, 128-byte swizzle.
+lf_status encode_cache_map(CUtensorMap* m, void* base, int D, int S, int units) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return fail(LF_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                          static_cast<cuuint64_t>(units)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                             static_cast<cuuint64_t>(S) * static_cast<cuuint64_t>(D) * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(lf::kBoxCols), static_cast<cuuint32_t>(lf::kTile), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(LF_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
+    return LF_OK;
+}
+
+// ---------------------------------------------------------------- planning --
+
+struct Plan {
+    int tiles, chunk_tiles, nchunk;
+};
+
+// Split the slot axis of every unit into nchunk chunks of chunk_tiles tiles:
+// enough CTAs to fill the GPU several times over, chunks as long as
+// possible, at most kMaxChunkTiles tiles and kMaxNChunk chunks.
+Plan plan_split(int S, int units, int sms) {
+    Plan pl;
+    pl.tiles = (S + lf::kTile - 1) / lf::kTile;
+    int nchunk = 0;
+    if (const char* env = std::getenv("LF_CHUNK_TILES")) {
+        const int ct = std::atoi(env);
+        if (ct >= 1 && ct <= lf::kMaxChunkTiles) nchunk = (pl.tiles + ct - 1) / ct;
+    }
+    if (nchunk == 0) {
+        const long target_ctas = 8L * sms;
+        nchunk = static_cast<int>((target_ctas + units - 1) / units);
+    }
+    nchunk = std::max(nchunk, (pl.tiles + lf::kMaxChunkTiles - 1) / lf::kMaxChunkTiles);
+    nchunk = std::min(std::max(nchunk, 1), std::min(pl.tiles, kMaxNChunk));
+    pl.chunk_tiles = (pl.tiles + nchunk - 1) / nchunk;
+    pl.nchunk = (pl.tiles + pl.chunk_tiles - 1) / pl.chunk_tiles;
+    return pl;
+}
+
+// ---------------------------------------------------------------- checking --
+
+struct Shape {
+    int B, Hq, Hkv, d, S, W;
+    float scale;
+};
+
+lf_status check_shape(const Shape& s) {
+    if (s.B < 1 || s.Hq < 1 || s.Hkv < 1 || s.d < 1 || s.S < 1)
+        return fail(LF_ERR_INVALID_ARG, "sizes must be >= 1 (B=%d Hq=%d Hkv=%d d=%d S=%d)", s.B, s.Hq, s.Hkv, s.d, s.S);
+    if (s.Hq % s.Hkv != 0) return fail(LF_ERR_INVALID_ARG, "Hq (%d) is not a multiple of Hkv (%d)", s.Hq, s.Hkv);
+    if (s.W < 0) return fail(LF_ERR_INVALID_ARG, "W must be >= 0 (got %d)", s.W);
+    if (!std::isfinite(s.scale)) return fail(LF_ERR_INVALID_ARG, "scale must be finite");
+    if (s.d != 64 && s.d != 128) return fail(LF_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", s.d);
+    const int g = s.Hq / s.Hkv;
+    if (g != 1 && g != 2 && g != 4 && g != 8)
+        return fail(LF_ERR_UNSUPPORTED, "group size Hq/Hkv = %d (supported: 1, 2, 4, 8)", g);
+    if (s.S > kMaxS) return fail(LF_ERR_UNSUPPORTED, "S = %d exceeds %d", s.S, kMaxS);
+    if (static_cast<long>(s.B) * s.Hkv > 65535)
+        return fail(LF_ERR_UNSUPPORTED, "B * Hkv = %ld exceeds 65535", static_cast<long>(s.B) * s.Hkv);
+    return LF_OK;
+}
+
+lf_status check_ptr(const void* p, size_t align, const char* name) {
+    if (!p) return fail(LF_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned(p, align)) return fail(LF_ERR_INVALID_ARG, "%s is not %zu-byte aligned", name, align);
+    return LF_OK;
+}
+
+struct StepArgs {
+    const void* q;
+    void* k_cache;
+    void* v_cache;
+    int32_t* mask;
+    const void* new_k;
+    const void* new_v;
+    const int32_t* write_slot;
+    void* out;
+    int32_t* next_slot;
+    float* scores;
+};
+
+lf_status check_args(const StepArgs& a, const Shape& s) {
+    lf_status st;
+    if ((st = check_ptr(a.q, 16, "q")) != LF_OK) return st;
+    if ((st = check_ptr(a.k_cache, 16, "k_cache")) != LF_OK) return st;
+    if ((st = check_ptr(a.v_cache, 16, "v_cache")) != LF_OK) return st;
+    if ((st = check_ptr(a.mask, 4, "mask")) != LF_OK) return st;
+    if ((st = check_ptr(a.new_k, 16, "new_k")) != LF_OK) return st;
+    if ((st = check_ptr(a.new_v, 16, "new_v")) != LF_OK) return st;
+    if ((st = check_ptr(a.write_slot, 4, "write_slot")) != LF_OK) return st;
+    if ((st = check_ptr(a.out, 16, "out")) != LF_OK) return st;
+    if ((st = check_ptr(a.next_slot, 4, "next_slot")) != LF_OK) return st;
+    if (a.scores && !aligned(a.scores, 4)) return fail(LF_ERR_INVALID_ARG, "scores is not 4-byte aligned");
+    return check_shape(s);
+}
+
+struct Layout {
+    size_t ml, o, stash, total;
+};
+
+Layout scratch_layout(const Shape& s, const Plan& pl, size_t extra) {
+    const size_t units = static_cast<size_t>(s.B) * s.Hkv;
+    const size_t g = static_cast<size_t>(s.Hq / s.Hkv);
+    Layout L;
+    L.ml = 0;
+    L.o = align_up(L.ml + units * pl.nchunk * g * sizeof(float2), 256);
+    L.stash = align_up(L.o + units * pl.nchunk * g * s.d * sizeof(float), 256);
+    L.total = align_up(L.stash + units * static_cast<size_t>(s.S) * g * sizeof(float), 256) + extra;
+    return L;
+}
+
+// Enqueue the two kernels of one step. Arguments are already checked.
+lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, Scratch* scr,
+                       const Layout& L, const Plan& pl) {
+    const int units = s.B * s.Hkv;
+    const int g = s.Hq / s.Hkv;
+    CUtensorMap tmK, tmV;
+    lf_status st = encode_cache_map(&tmK, a.k_cache, s.d, s.S, units);
+    if (st != LF_OK) return st;
+    if ((st = encode_cache_map(&tmV, a.v_cache, s.d, s.S, units)) != LF_OK) return st;
+
+    char* base = static_cast<char*>(scr->base);
+    lf::SplitParams sp;
+    sp.q = static_cast<const __nv_bfloat16*>(a.q);
+    sp.k_cache = static_cast<__nv_bfloat16*>(a.k_cache);
+    sp.v_cache = static_cast<__nv_bfloat16*>(a.v_cache);
+    sp.mask = a.mask;
+    sp.new_k = static_cast<const __nv_bfloat16*>(a.new_k);
+    sp.new_v = static_cast<const __nv_bfloat16*>(a.new_v);
+    sp.write_slot = a.write_slot;
+    sp.part_o = reinterpret_cast<float*>(base + L.o);
+    sp.part_ml = reinterpret_cast<float2*>(base + L.ml);
+    sp.stash = reinterpret_cast<float*>(base + L.stash);
+    sp.dev_err = scr->dev_err;
+    sp.Hq = s.Hq;
+    sp.Hkv = s.Hkv;
+    sp.S = s.S;
+    sp.W = s.W;
+    sp.nchunk = pl.nchunk;
+    sp.chunk_tiles = pl.chunk_tiles;
+    sp.scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
+
+    lf::CombineParams cp;
+    cp.part_o = sp.part_o;
+    cp.part_ml = sp.part_ml;
+    cp.stash = sp.stash;
+    cp.mask = a.mask;
+    cp.out = static_cast<__nv_bfloat16*>(a.out);
+    cp.next_slot = a.next_slot;
+    cp.scores = a.scores;
+    cp.Hq = s.Hq;
+    cp.Hkv = s.Hkv;
+    cp.S = s.S;
+    cp.W = s.W;
+    cp.nchunk = pl.nchunk;
+
+    cudaError_t e;
+    {
+        ProfScope prof(LF_KERNEL_ATTN_SPLIT, stream);
+        e = lf::launch_attn_split(s.d, g, tmK, tmV, sp, units, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "split attention launch");
+    {
+        ProfScope prof(LF_KERNEL_COMBINE, stream);
+        e = lf::launch_combine(s.d, g, cp, units, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    return LF_OK;
+}
+
+lf_status run_step(const StepArgs& a, const Shape& s, void* stream_v) {
+    lf_status st = check_args(a, s);
+    if (st != LF_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const Plan pl = plan_split(s.S, s.B * s.Hkv, sm_count(dev));
+    const Layout L = scratch_layout(s, pl, 0);
+    Scratch* scr = nullptr;
+    if ((st = get_scratch(dev, stream, L.total, &scr)) != LF_OK) return st;
+    g_last_error[0] = '\0';
+    return enqueue_step(a, s, stream, scr, L, pl);
+}
+
+}  // namespace
+
+extern "C" {
+
+lf_status lf_decode_step(const void* q, void* k_cache, void* v_cache, int32_t* mask,
+                         const void* new_k, const void* new_v, const int32_t* write_slot,
+                         void* out, int32_t* next_slot, int B, int Hq, int Hkv, int d, int S,
+                         int W, float scale, void* stream) {
+    StepArgs a{q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slot, nullptr};
+    return run_step(a, Shape{B, Hq, Hkv, d, S, W, scale}, stream);
+}
+
+lf_status lf_decode_step_scores(const void* q, void* k_cache, void* v_cache, int32_t* mask,
+                                const void* new_k, const void* new_v,
+                                const int32_t* write_slot, void* out, int32_t* next_slot,
+                                float* scores, int B, int Hq, int Hkv, int d, int S, int W,
+                                float scale, void* stream) {
+    if (!scores) return fail(LF_ERR_INVALID_ARG, "scores is NULL");
+    StepArgs a{q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slot, scores};
+    return run_step(a, Shape{B, Hq, Hkv, d, S, W, scale}, stream);
+}
+
+lf_status lf_decode_step_host(const void* q_host, void* k_cache, void* v_cache, int32_t* mask,
+                              const void* new_k_host, const void* new_v_host,
+                              const int32_t* write_slot_host, void* out_host,
+                              int32_t* next_slot_host, int B, int Hq, int Hkv, int d, int S,
+                              int W, float scale, void* stream_v) {
+    const Shape s{B, Hq, Hkv, d, S, W, scale};
+    // Host buffers need no device alignment; the device staging copies are aligned.
+    lf_status st;
+    if (!q_host || !new_k_host || !new_v_host || !write_slot_host || !out_host || !next_slot_host)
+        return fail(LF_ERR_INVALID_ARG, "a host buffer is NULL");
+    if ((st = check_ptr(k_cache, 16, "k_cache")) != LF_OK) return st;
+    if ((st = check_ptr(v_cache, 16, "v_cache")) != LF_OK) return st;
+    if ((st = check_ptr(mask, 4, "mask")) != LF_OK) return st;
+    if ((st = check_shape(s)) != LF_OK) return st;
+
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const size_t units = static_cast<size_t>(B) * Hkv;
+    const size_t q_bytes = static_cast<size_t>(B) * Hq * d * 2;
+    const size_t kv_bytes = units * d * 2;
+    const size_t i_bytes = units * 4;
+    size_t off_q = 0, off_k = align_up(off_q + q_bytes, 256), off_v = align_up(off_k + kv_bytes, 256),
+           off_w = align_up(off_v + kv_bytes, 256), off_o = align_up(off_w + i_bytes, 256),
+           off_n = align_up(off_o + q_bytes, 256), staging = align_up(off_n + i_bytes, 256);
+    const Plan pl = plan_split(S, static_cast<int>(units), sm_count(dev));
+    const Layout L = scratch_layout(s, pl, staging);
+    Scratch* scr = nullptr;
+    if ((st = get_scratch(dev, stream, L.total, &scr)) != LF_OK) return st;
+    char* stg = static_cast<char*>(scr->base) + (L.total - staging);
+    StepArgs a{stg + off_q, k_cache, v_cache, mask, stg + off_k, stg + off_v,
+               reinterpret_cast<int32_t*>(stg + off_w), stg + off_o,
+               reinterpret_cast<int32_t*>(stg + off_n), nullptr};
+    g_last_error[0] = '\0';
+    if ((e = cudaMemcpyAsync(stg + off_q, q_host, q_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(stg + off_k, new_k_host, kv_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(stg + off_v, new_v_host, kv_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(stg + off_w, write_slot_host, i_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        return cuda_fail(e, "host-to-device copy");
+    if ((st = enqueue_step(a, s, stream, scr, L, pl)) != LF_OK) return st;
+    if ((e = cudaMemcpyAsync(out_host, stg + off_o, q_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(next_slot_host, stg + off_n, i_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+        return cuda_fail(e, "device-to-host copy");
+    return LF_OK;
+}
+
+lf_status lf_device_errors(void* stream_v, uint32_t* flags, int clear) {
+    if (!flags) return fail(LF_ERR_INVALID_ARG, "flags is NULL");
+    *flags = 0;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    uint32_t* word = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_scratch.find({dev, stream});
+        if (it == g_scratch.end() || !it->second.dev_err) return LF_OK;
+        word = it->second.dev_err;
+    }
+    uint32_t v = 0;
+    if ((e = cudaMemcpyAsync(&v, word, sizeof v, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+        return cuda_fail(e, "reading the device error word");
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    *flags = v;
+    if (clear && v) {
+        if ((e = cudaMemsetAsync(word, 0, sizeof v, stream)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+        if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    }
+    return LF_OK;
+}
+
+lf_status lf_profile_enable(int enabled) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof_on = enabled != 0;
+    return LF_OK;
+}
+
+lf_status lf_profile_collect(int kernel_id, double* total_ms, int64_t* launches) {
+    if (!total_ms || !launches) return fail(LF_ERR_INVALID_ARG, "NULL output");
+    if (kernel_id < 0 || kernel_id >= LF_KERNEL_COUNT) return fail(LF_ERR_INVALID_ARG, "bad kernel id %d", kernel_id);
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    double sum = 0.0;
+    int64_t n = 0;
+    std::vector<ProfRec> keep;
+    for (const ProfRec& r : g_prof) {
+        if (r.kernel != kernel_id) {
+            keep.push_back(r);
+            continue;
+        }
+        cudaError_t e = cudaEventSynchronize(r.stop);
+        float ms = 0.f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
+        if (e != cudaSuccess) return cuda_fail(e, "profile event");
+        sum += ms;
+        ++n;
+        g_event_pool.push_back(r.start);
+        g_event_pool.push_back(r.stop);
+    }
+    g_prof.swap(keep);
+    *total_ms = sum;
+    *launches = n;
+    return LF_OK;
+}
+
+lf_status lf_release_workspace(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto& kv : g_scratch) {
+        cudaSetDevice(kv.first.first);
+        cudaDeviceSynchronize();
+        if (kv.second.base) cudaFree(kv.second.base);
+        if (kv.second.dev_err) cudaFree(kv.second.dev_err);
+    }
+    g_scratch.clear();
+    cudaSetDevice(cur);
+    return LF_OK;
+}
+
+const char* lf_status_string(lf_status status) {
+    switch (status) {
+        case LF_OK: return "LF_OK";
+        case LF_ERR_INVALID_ARG: return "LF_ERR_INVALID_ARG: invalid argument";
+        case LF_ERR_UNSUPPORTED: return "LF_ERR_UNSUPPORTED: shape not supported";
+        case LF_ERR_CUDA: return "LF_ERR_CUDA: CUDA error";
+        case LF_ERR_NO_MEMORY: return "LF_ERR_NO_MEMORY: scratch allocation failed";
+    }
+    return "unknown lf_status";
+}
+
+const char* lf_last_error(void) { return g_last_error; }
+
+int lf_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,161 @@
+/*
+ * lf_decode.h - C ABI of the GB300 (sm_103a) LongFlow decode-step library.
+ *
+ * One call performs one decode step of "LongFlow: Efficient KV Cache
+ * Compression for Reasoning Models" for every (sequence b, KV head kvh) unit
+ * of a batch:
+ *
+ *   1. Slot write (Fig. 2, Left): the current token's K/V row replaces the
+ *      cache slot chosen at the previous step (write_slot). That slot's age
+ *      becomes 0, every other live slot of the unit ages by one.
+ *   2. Attention (Fig. 2, Middle): the g = Hq / Hkv query heads of the unit
+ *      attend over the static, mask-gated cache with softmax(scale * q.k).
+ *   3. LongFlowScore and eviction (Fig. 2, Right; Fig. 1 caption): P.V is
+ *      split into G[h][j][c] = p[h][j] * v[j][c] and O = sum_j G. The paper
+ *      prints no formula for the score; this library uses
+ *          I_j = sum over the unit's heads h, sum over c, of |p[h][j] * v[j][c]|
+ *      with p the final normalised weight. The returned slot is the argmin of
+ *      I_j over live slots whose age is at least W (the W most recent tokens
+ *      are protected), ties to the lowest index.
+ *
+ * Conventions shared by every entry point:
+ *   - bf16 arrays are raw IEEE bfloat16 (uint16 bit patterns), row-major,
+ *     contiguous. Layouts:
+ *        q, out          [B][Hq][d]
+ *        k_cache,v_cache [B][Hkv][S][d]
+ *        new_k, new_v    [B][Hkv][d]
+ *        mask            [B][Hkv][S] int32
+ *        write_slot,
+ *        next_slot       [B][Hkv]   int32
+ *   - Query head h belongs to KV head floor(h / g).
+ *   - mask: a negative entry marks an empty/masked slot (never attended, never
+ *     returned); an entry >= 0 is the slot's age in decode steps.
+ *   - write_slot = -1 means "no write" (a priming call: nothing ages). A value
+ *     in [0, S) is written even into a masked slot, which becomes live with
+ *     age 0 (that is how a caller fills an empty cache). Any other value is
+ *     ignored and raises LF_DEVERR_BAD_WRITE_SLOT in the device error word.
+ *   - next_slot = -1 when no slot is eligible.
+ *   - A unit with no live slot writes an all-zero output row.
+ *   - All device pointers belong to the caller and must stay valid until the
+ *     stream reaches the end of the call's work. bf16 arrays must be 16-byte
+ *     aligned, int32 arrays 4-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream). Results are valid once the stream has synchronised.
+ *   - The library owns a per-(device, stream) scratch buffer that it grows on
+ *     demand with cudaMalloc (released by lf_release_workspace). Calls on the
+ *     same stream are ordered; calls on different streams use different
+ *     scratch.
+ *   - Argument errors are detected on the host before anything is enqueued;
+ *     the kernels never trap.
+ *
+ * Supported shapes: d in {64, 128}; g in {1, 2, 4, 8}; 1 <= S <= 2^20;
+ * B * Hkv <= 65535. Anything else returns LF_ERR_UNSUPPORTED.
+ */
+#ifndef LF_DECODE_H
+#define LF_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum lf_status {
+    LF_OK = 0,
+    LF_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, Hq % Hkv != 0, W < 0, ... */
+    LF_ERR_UNSUPPORTED = 2, /* valid request outside the supported shapes */
+    LF_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    LF_ERR_NO_MEMORY = 4    /* scratch allocation failed */
+} lf_status;
+
+/* Bits of the device error word (lf_device_errors). */
+#define LF_DEVERR_BAD_WRITE_SLOT 0x1u /* a write_slot outside [-1, S) was ignored */
+#define LF_DEVERR_WAIT_TIMEOUT 0x2u   /* a pipeline wait gave up; that step's results are invalid */
+
+/* Kernel ids for lf_profile_collect. */
+#define LF_KERNEL_ATTN_SPLIT 0 /* slot write + mask ageing + split attention + score terms */
+#define LF_KERNEL_COMBINE 1    /* split merge + output + LongFlowScore + argmin */
+#define LF_KERNEL_COUNT 2
+
+/*
+ * One decode step (all three stages above) on device buffers.
+ *
+ * q         in   bf16 [B][Hq][d]       current queries (post-RoPE; the op applies none)
+ * k_cache   in/out bf16 [B][Hkv][S][d] static K cache; row write_slot is overwritten
+ * v_cache   in/out bf16 [B][Hkv][S][d] static V cache; row write_slot is overwritten
+ * mask      in/out int32 [B][Hkv][S]   ages (>= 0) or masked (< 0); aged in place
+ * new_k     in   bf16 [B][Hkv][d]      the current token's K row per unit
+ * new_v     in   bf16 [B][Hkv][d]      the current token's V row per unit
+ * write_slot in  int32 [B][Hkv]        slot to overwrite (the previous next_slot), or -1
+ * out       out  bf16 [B][Hq][d]       attention output, round-to-nearest-even
+ * next_slot out  int32 [B][Hkv]        slot to overwrite at the next step, or -1
+ * W              protected window: slots with age < W are never returned (W >= 0)
+ * scale          logit multiplier (typically 1/sqrt(d)); must be finite
+ * stream         cudaStream_t to enqueue on
+ */
+lf_status lf_decode_step(const void* q, void* k_cache, void* v_cache, int32_t* mask,
+                         const void* new_k, const void* new_v, const int32_t* write_slot,
+                         void* out, int32_t* next_slot, int B, int Hq, int Hkv, int d, int S,
+                         int W, float scale, void* stream);
+
+/*
+ * lf_decode_step plus the per-slot LongFlowScore, for inspection and tests.
+ * scores out float [B][Hkv][S]: I_j on every live slot (protected ones
+ * included), +inf on masked slots. Same semantics otherwise.
+ */
+lf_status lf_decode_step_scores(const void* q, void* k_cache, void* v_cache, int32_t* mask,
+                                const void* new_k, const void* new_v,
+                                const int32_t* write_slot, void* out, int32_t* next_slot,
+                                float* scores, int B, int Hq, int Hkv, int d, int S, int W,
+                                float scale, void* stream);
+
+/*
+ * One decode step whose per-step inputs and outputs live in HOST memory, for
+ * callers that drive decoding from the CPU. q, new_k, new_v and write_slot are
+ * copied host -> device, the step runs, and out and next_slot are copied
+ * device -> host, all enqueued on `stream` (pinned host buffers make the copies
+ * asynchronous). The caches and the mask stay on the device (device pointers),
+ * as they are the decoder's resident state. The host output buffers are valid
+ * after the stream synchronises. Staging lives in the library's scratch.
+ */
+lf_status lf_decode_step_host(const void* q_host, void* k_cache, void* v_cache, int32_t* mask,
+                              const void* new_k_host, const void* new_v_host,
+                              const int32_t* write_slot_host, void* out_host,
+                              int32_t* next_slot_host, int B, int Hq, int Hkv, int d, int S,
+                              int W, float scale, void* stream);
+
+/*
+ * Read (and optionally clear) the device error word of `stream`'s scratch.
+ * Synchronises the stream. *flags receives an OR of LF_DEVERR_* bits, 0 if the
+ * stream has never run a step.
+ */
+lf_status lf_device_errors(void* stream, uint32_t* flags, int clear);
+
+/*
+ * Kernel timing. While enabled, every kernel launch of the library is
+ * bracketed by CUDA events recorded on its own stream. lf_profile_collect
+ * synchronises those events and returns, for one kernel id, the summed event
+ * time in milliseconds and the number of launches since the last collect for
+ * that id, then forgets them.
+ */
+lf_status lf_profile_enable(int enabled);
+lf_status lf_profile_collect(int kernel_id, double* total_ms, int64_t* launches);
+
+/* Free every scratch buffer (after synchronising the device of each). */
+lf_status lf_release_workspace(void);
+
+/* Static description of a status code. */
+const char* lf_status_string(lf_status status);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* lf_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int lf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LF_DECODE_H */

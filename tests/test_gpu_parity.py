@@ -1,0 +1,137 @@
+"""GPU parity: the CUDA decode step against the fp64 oracle on the seeded
+workloads, step after step.
+
+Small workloads are compared element by element on every unit. The three
+large workloads run at full size in the launch configuration the benchmark
+times; the oracle checks a sample of (b, kvh) units one by one, and every unit
+is checked for the properties that hold at any size (eligible, never
+protected, never masked). Both sides write the oracle's chosen slot at the
+next step, so their states stay identical.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import decode_kv_cache_step_gb300 as lf
+from decode_kv_cache_step_gb300.workloads import WORKLOADS, initial_state, step_inputs
+
+from _gpu import DevState, compare_unit, oracle_step, to_host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample_units(wl, n, seed=0):
+    rng = np.random.default_rng(seed)
+    units = {0, wl.units - 1}
+    units.update(int(x) for x in rng.choice(wl.units, size=min(n, wl.units), replace=False))
+    return sorted(units)
+
+
+def run_parity(wl, steps, sample=None, check_scores=True):
+    st = initial_state(wl)
+    dev = DevState(st["k_cache"], st["v_cache"], st["mask"], wl.Hq)
+    host = {k: st[k] for k in ("k_cache", "v_cache", "mask")}
+    ws = np.full((wl.B, wl.Hkv), -1, dtype=np.int32)
+    units = list(range(wl.units)) if sample is None else sample
+    worst = {"out_err": 0.0, "score_rel": 0.0, "exact_next": 0, "checked": 0}
+    for t in range(steps + 1):
+        inp = step_inputs(wl, t)
+        gpu = dev.step(inp["q"], inp["new_k"], inp["new_v"], ws, wl.W, wl.scale, scores=check_scores)
+        ora = oracle_step(host, inp["q"], inp["new_k"], inp["new_v"], ws, wl.W, wl.scale,
+                          units=None if sample is None else units)
+        mask_gpu = dev.mask.cpu().numpy()
+        for u in units:
+            b, kvh = divmod(u, wl.Hkv)
+            # state after the write: bit-exact
+            assert np.array_equal(mask_gpu[b, kvh], host["mask"][b, kvh]), f"step {t}: mask ({b},{kvh})"
+            if ws[b, kvh] >= 0:
+                s = int(ws[b, kvh])
+                assert np.array_equal(to_host_bits(dev.k[b, kvh, s]), host["k_cache"][b, kvh, s])
+                assert np.array_equal(to_host_bits(dev.v[b, kvh, s]), host["v_cache"][b, kvh, s])
+            stt = compare_unit(gpu, ora, b, kvh, wl.g, host["mask"], wl.W, check_scores=check_scores,
+                               where=f"{wl.name} step {t}")
+            worst["out_err"] = max(worst["out_err"], stt["out_err"])
+            worst["score_rel"] = max(worst["score_rel"], stt.get("score_rel", 0.0))
+            worst["exact_next"] += int(stt.get("exact_next", True))
+            worst["checked"] += 1
+        # properties on every unit
+        nxt = gpu["next_slot"]
+        live_elig = mask_gpu >= wl.W
+        for u in range(wl.units):
+            b, kvh = divmod(u, wl.Hkv)
+            n = int(nxt[b, kvh])
+            if n == -1:
+                assert not live_elig[b, kvh].any(), f"step {t}: unit ({b},{kvh}) returned -1"
+            else:
+                assert 0 <= n < wl.S and live_elig[b, kvh, n], f"step {t}: unit ({b},{kvh}) slot {n}"
+        ws = nxt.astype(np.int32).copy()
+        for u in units:
+            b, kvh = divmod(u, wl.Hkv)
+            ws[b, kvh] = ora["next_slot"][b, kvh]
+    assert lf.device_errors() == 0
+    return worst
+
+
+def test_parity_tiny_every_step():
+    wl = WORKLOADS["tiny_b2_s256"]
+    worst = run_parity(wl, wl.steps)
+    assert worst["checked"] == (wl.steps + 1) * wl.units
+
+
+def test_parity_qwen3_b1_s2400_every_step():
+    wl = WORKLOADS["qwen3_8b_b1_s2400"]
+    worst = run_parity(wl, wl.steps)
+    assert worst["checked"] == (wl.steps + 1) * wl.units
+
+
+@pytest.mark.parametrize("name", ["qwen3_8b_b128_s3200", "llama8b_b256_s2400_ragged",
+                                  "long_b32_s16384_ragged"])
+def test_parity_full_size_sampled(name):
+    wl = WORKLOADS[name]
+    run_parity(wl, steps=3, sample=_sample_units(wl, 14, seed=len(name)))
+
+
+def test_scoreless_entry_point_matches_scores_variant():
+    """lf_decode_step (what the benchmark times) and lf_decode_step_scores give
+    the same output and slot, bit for bit."""
+    wl = WORKLOADS["qwen3_8b_b128_s3200"].with_batch(16)
+    st = initial_state(wl)
+    inp = step_inputs(wl, 1)
+    ws = np.random.default_rng(0).integers(0, wl.S, size=(wl.B, wl.Hkv)).astype(np.int32)
+    a = DevState(st["k_cache"], st["v_cache"], st["mask"], wl.Hq)
+    b = DevState(st["k_cache"], st["v_cache"], st["mask"], wl.Hq)
+    ra = a.step(inp["q"], inp["new_k"], inp["new_v"], ws, wl.W, wl.scale, scores=True)
+    rb = b.step(inp["q"], inp["new_k"], inp["new_v"], ws, wl.W, wl.scale, scores=False)
+    assert np.array_equal(ra["out"], rb["out"])
+    assert np.array_equal(ra["next_slot"], rb["next_slot"])
+    assert torch.equal(a.mask, b.mask) and torch.equal(a.k, b.k) and torch.equal(a.v, b.v)
+
+
+def test_host_io_entry_point_matches_device_entry_point():
+    wl = WORKLOADS["llama8b_b256_s2400_ragged"].with_batch(8)
+    st = initial_state(wl)
+    inp = step_inputs(wl, 2)
+    ws = np.full((wl.B, wl.Hkv), 5, dtype=np.int32)
+    a = DevState(st["k_cache"], st["v_cache"], st["mask"], wl.Hq)
+    b = DevState(st["k_cache"], st["v_cache"], st["mask"], wl.Hq)
+    ra = a.step(inp["q"], inp["new_k"], inp["new_v"], ws, wl.W, wl.scale, scores=False)
+    pin = lambda x: torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x).pin_memory()
+    q, nk, nv, w = pin(inp["q"]), pin(inp["new_k"]), pin(inp["new_v"]), pin(ws)
+    q, nk, nv = q.view(torch.bfloat16), nk.view(torch.bfloat16), nv.view(torch.bfloat16)
+    out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.bfloat16).pin_memory()
+    nxt = torch.empty((wl.B, wl.Hkv), dtype=torch.int32).pin_memory()
+    lf.decode_step_host(q, b.k, b.v, b.mask, nk, nv, w, out, nxt, wl.W, wl.scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.float().numpy().astype(np.float64), ra["out"])
+    assert np.array_equal(nxt.numpy(), ra["next_slot"])
+    assert torch.equal(a.mask, b.mask) and torch.equal(a.k, b.k)
+
+
+@pytest.mark.parametrize("chunk_tiles", ["1", "3", "32"])
+def test_split_shapes_do_not_change_results(monkeypatch, chunk_tiles):
+    """Different slot-axis splits give results within tolerance of the oracle."""
+    monkeypatch.setenv("LF_CHUNK_TILES", chunk_tiles)
+    wl = WORKLOADS["long_b32_s16384_ragged"].with_batch(2)
+    run_parity(wl, steps=2)

@@ -43,20 +43,20 @@ from decode_kv_cache_step_gb300.workloads import (  # noqa: E402
 METRIC = "decode steps/s and achieved HBM GB/s (% of GB300 peak) for fused attn+score+evict"
 DEFAULT_WORKLOAD = "qwen3_8b_b128_s3200"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "lf_attn_split_kernel.qwen3_8b_b128_s3200.md")
-SPLIT_SOURCES = ["lf_attn_split.cu", "lf_ptx.cuh", "lf_kernels.h"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "lf_decode_step_kernel.qwen3_8b_b128_s3200.md")
+KERNEL_SOURCES = ["lf_decode_step.cu", "lf_ptx.cuh", "lf_kernels.h"]
 
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in SPLIT_SOURCES:
+    for name in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "decode_kv_cache_step_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def committed_traffic():
-    """dram read+write bytes per launch of the split kernel from the committed ncu
+    """dram read+write bytes per launch of the decode-step kernel from the committed ncu
     summary, or None if absent or taken on another version of the kernel."""
     try:
         with open(PROFILE_SUMMARY) as fh:
@@ -284,8 +284,7 @@ def bench_lf(args, wl):
     # ---------------------------------------------------------- device-timed
     clocks = ClockSampler(local)
     time.sleep(0.3)
-    lf.profile_collect(lf.LF_KERNEL_ATTN_SPLIT)
-    lf.profile_collect(lf.LF_KERNEL_COMBINE)
+    lf.profile_collect(lf.LF_KERNEL_DECODE_STEP)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -301,8 +300,7 @@ def bench_lf(args, wl):
     t_wall1 = clocks.mark()
     lf.profile_enable(False)
     ms_total = ev0.elapsed_time(ev1)
-    split_ms, split_n = lf.profile_collect(lf.LF_KERNEL_ATTN_SPLIT)
-    comb_ms, comb_n = lf.profile_collect(lf.LF_KERNEL_COMBINE)
+    kern_ms, kern_n = lf.profile_collect(lf.LF_KERNEL_DECODE_STEP)
     if world > 1:
         t = torch.tensor([ms_total], dtype=torch.float64, device=device)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -359,12 +357,10 @@ def bench_lf(args, wl):
     ms_per_step = ms_total / args.steps
     value = world * args.steps / (ms_total / 1e3)
     alg = algorithmic_bytes(wl, lengths)
-    out_bytes = wl.B * wl.Hq * wl.d * 2
-    split_alg = alg - out_bytes          # the split kernel writes no output rows
-    split_avg_ms = split_ms / max(split_n, 1)
+    kern_avg_ms = kern_ms / max(kern_n, 1)
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    achieved = split_alg / (split_avg_ms / 1e3) / 1e9
+    achieved = alg / (kern_avg_ms / 1e3) / 1e9
     step_gbs = alg / (ms_per_step / 1e3) / 1e9
     line = {
         "metric": METRIC,
@@ -383,17 +379,16 @@ def bench_lf(args, wl):
         "hbm": {"algorithmic_bytes_per_step": alg, "achieved_gbs": step_gbs,
                 "frac_of_measured_peak": step_gbs / peak, "frac_of_8000_gbs": step_gbs / 8000.0,
                 "peak_kind": peak_kind},
-        "roofline": {"kernel": "lf_attn_split_kernel", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": "lf_decode_step_kernel", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": committed_traffic(), "algorithmic_bytes_per_launch": split_alg,
-                     "avg_launch_ms": split_avg_ms, "launches": split_n,
-                     "combine_avg_ms": comb_ms / max(comb_n, 1),
+                     "traffic": committed_traffic(), "algorithmic_bytes_per_launch": alg,
+                     "avg_launch_ms": kern_avg_ms, "launches": kern_n,
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "cpu_baseline": cpu,
         "e2e": {"value": world * args.steps / e2e_s, "unit": "steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "lf_decode_step_host from pinned host buffers; stream sync every step"},
-        "gpu_launches": split_n + comb_n,
+        "gpu_launches": kern_n,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
     print(json.dumps(line), flush=True)
@@ -408,6 +403,8 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--batch", type=int, default=None,
+                    help="run the first BATCH sequences of the workload (small profiling cases)")
     ap.add_argument("--impl", default="lf", choices=["lf", "reference"])
     ap.add_argument("--reference-units", type=int, default=64,
                     help="(b,kvh) units the reference arm runs per step")
@@ -416,6 +413,8 @@ def main():
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps, always
     wl = WORKLOADS[args.workload]
+    if args.batch is not None:
+        wl = wl.with_batch(args.batch)
     if args.impl == "reference":
         return bench_reference(args, wl)
     return bench_lf(args, wl)

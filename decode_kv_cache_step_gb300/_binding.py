@@ -25,9 +25,8 @@ LF_ERR_NO_MEMORY = 4
 LF_DEVERR_BAD_WRITE_SLOT = 0x1
 LF_DEVERR_WAIT_TIMEOUT = 0x2
 
-LF_KERNEL_ATTN_SPLIT = 0
-LF_KERNEL_COMBINE = 1
-KERNEL_NAMES = {LF_KERNEL_ATTN_SPLIT: "lf_attn_split_kernel", LF_KERNEL_COMBINE: "lf_combine_kernel"}
+LF_KERNEL_DECODE_STEP = 0
+KERNEL_NAMES = {LF_KERNEL_DECODE_STEP: "lf_decode_step_kernel"}
 
 # Every exported symbol of include/lf_decode.h.
 EXPORTED = (

@@ -46,15 +46,31 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 struct Scratch {
     void* base = nullptr;
     size_t bytes = 0;
-    uint32_t* dev_err = nullptr;  // never moves once created
+    uint32_t* dev_err = nullptr;   // never moves once created
+    uint32_t* arrivals = nullptr;  // per-unit chunk arrival counters, 0 between steps
+    size_t arrivals_len = 0;
 };
 
 std::mutex g_mu;
 std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
 
-lf_status get_scratch(int dev, cudaStream_t stream, size_t need, Scratch** out) {
+lf_status get_scratch(int dev, cudaStream_t stream, size_t need, size_t units, Scratch** out) {
     std::lock_guard<std::mutex> lock(g_mu);
     Scratch& s = g_scratch[{dev, stream}];
+    if (s.arrivals_len < units) {
+        if (s.arrivals) {
+            cudaError_t e = cudaStreamSynchronize(stream);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+            cudaFree(s.arrivals);
+            s.arrivals = nullptr;
+            s.arrivals_len = 0;
+        }
+        cudaError_t e = cudaMalloc(&s.arrivals, units * sizeof(uint32_t));
+        if (e != cudaSuccess) return fail(LF_ERR_NO_MEMORY, "cudaMalloc(arrival counters): %s", cudaGetErrorString(e));
+        e = cudaMemset(s.arrivals, 0, units * sizeof(uint32_t));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+        s.arrivals_len = units;
+    }
     if (!s.dev_err) {
         cudaError_t e = cudaMalloc(&s.dev_err, 256);
         if (e != cudaSuccess) return fail(LF_ERR_NO_MEMORY, "cudaMalloc(error word): %s", cudaGetErrorString(e));
@@ -269,7 +285,7 @@ Layout scratch_layout(const Shape& s, const Plan& pl, size_t extra) {
     return L;
 }
 
-// Enqueue the two kernels of one step. Arguments are already checked.
+// Enqueue one step. Arguments are already checked.
 lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, Scratch* scr,
                        const Layout& L, const Plan& pl) {
     const int units = s.B * s.Hkv;
@@ -280,7 +296,7 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
     if ((st = encode_cache_map(&tmV, a.v_cache, s.d, s.S, units)) != LF_OK) return st;
 
     char* base = static_cast<char*>(scr->base);
-    lf::SplitParams sp;
+    lf::StepParams sp;
     sp.q = static_cast<const __nv_bfloat16*>(a.q);
     sp.k_cache = static_cast<__nv_bfloat16*>(a.k_cache);
     sp.v_cache = static_cast<__nv_bfloat16*>(a.v_cache);
@@ -288,9 +304,13 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
     sp.new_k = static_cast<const __nv_bfloat16*>(a.new_k);
     sp.new_v = static_cast<const __nv_bfloat16*>(a.new_v);
     sp.write_slot = a.write_slot;
+    sp.out = static_cast<__nv_bfloat16*>(a.out);
+    sp.next_slot = a.next_slot;
+    sp.scores = a.scores;
     sp.part_o = reinterpret_cast<float*>(base + L.o);
     sp.part_ml = reinterpret_cast<float2*>(base + L.ml);
     sp.stash = reinterpret_cast<float*>(base + L.stash);
+    sp.arrivals = scr->arrivals;
     sp.dev_err = scr->dev_err;
     sp.Hq = s.Hq;
     sp.Hkv = s.Hkv;
@@ -300,31 +320,12 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
     sp.chunk_tiles = pl.chunk_tiles;
     sp.scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
 
-    lf::CombineParams cp;
-    cp.part_o = sp.part_o;
-    cp.part_ml = sp.part_ml;
-    cp.stash = sp.stash;
-    cp.mask = a.mask;
-    cp.out = static_cast<__nv_bfloat16*>(a.out);
-    cp.next_slot = a.next_slot;
-    cp.scores = a.scores;
-    cp.Hq = s.Hq;
-    cp.Hkv = s.Hkv;
-    cp.S = s.S;
-    cp.W = s.W;
-    cp.nchunk = pl.nchunk;
-
     cudaError_t e;
     {
-        ProfScope prof(LF_KERNEL_ATTN_SPLIT, stream);
-        e = lf::launch_attn_split(s.d, g, tmK, tmV, sp, units, stream);
+        ProfScope prof(LF_KERNEL_DECODE_STEP, stream);
+        e = lf::launch_decode_step(s.d, g, tmK, tmV, sp, units, stream);
     }
-    if (e != cudaSuccess) return cuda_fail(e, "split attention launch");
-    {
-        ProfScope prof(LF_KERNEL_COMBINE, stream);
-        e = lf::launch_combine(s.d, g, cp, units, stream);
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");
     return LF_OK;
 }
 
@@ -338,7 +339,7 @@ lf_status run_step(const StepArgs& a, const Shape& s, void* stream_v) {
     const Plan pl = plan_split(s.S, s.B * s.Hkv, sm_count(dev));
     const Layout L = scratch_layout(s, pl, 0);
     Scratch* scr = nullptr;
-    if ((st = get_scratch(dev, stream, L.total, &scr)) != LF_OK) return st;
+    if ((st = get_scratch(dev, stream, L.total, static_cast<size_t>(s.B) * s.Hkv, &scr)) != LF_OK) return st;
     g_last_error[0] = '\0';
     return enqueue_step(a, s, stream, scr, L, pl);
 }
@@ -394,7 +395,7 @@ lf_status lf_decode_step_host(const void* q_host, void* k_cache, void* v_cache, 
     const Plan pl = plan_split(S, static_cast<int>(units), sm_count(dev));
     const Layout L = scratch_layout(s, pl, staging);
     Scratch* scr = nullptr;
-    if ((st = get_scratch(dev, stream, L.total, &scr)) != LF_OK) return st;
+    if ((st = get_scratch(dev, stream, L.total, static_cast<size_t>(s.B) * s.Hkv, &scr)) != LF_OK) return st;
     char* stg = static_cast<char*>(scr->base) + (L.total - staging);
     StepArgs a{stg + off_q, k_cache, v_cache, mask, stg + off_k, stg + off_v,
                reinterpret_cast<int32_t*>(stg + off_w), stg + off_o,
@@ -480,6 +481,7 @@ lf_status lf_release_workspace(void) {
         cudaDeviceSynchronize();
         if (kv.second.base) cudaFree(kv.second.base);
         if (kv.second.dev_err) cudaFree(kv.second.dev_err);
+        if (kv.second.arrivals) cudaFree(kv.second.arrivals);
     }
     g_scratch.clear();
     cudaSetDevice(cur);

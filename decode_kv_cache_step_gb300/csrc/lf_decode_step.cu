@@ -1,20 +1,25 @@
-// Split attention kernel of the LongFlow decode step (sm_103a).
+// The LongFlow decode-step kernel (sm_103a): slot write, split-KV attention,
+// LongFlowScore and eviction in one launch.
 //
 // "LongFlow: Efficient KV Cache Compression for Reasoning Models":
-//   Fig. 2 (Left)   the current K/V covers the slot chosen at the previous step;
+//   Fig. 2 (Left)   the current K/V covers the slot chosen at the previous step,
+//                   then the static KV and Mask go to the kernel with Q, which
+//                   returns the output and the slot to cover next;
 //   Fig. 2 (Middle) K, V and the Mask stream from HBM into on-chip memory by
 //                   block and the attention runs there;
 //   Fig. 2 (Right)  P.V is split in two: G = p * v (per slot) and O = sum_j G.
 //                   LongFlowScore is read off G. With the score
 //                   I_j = sum_h sum_c |p_hj v_jc| = (sum_h p_hj) * ||v_j||_1
 //                   (p >= 0), G never has to exist: each live slot leaves
-//                   log2(p~_hj) + log2(||v_j||_1) per head, relative to this
-//                   chunk's final max, and the combine kernel rescales it.
+//                   t_hj = log2(exp(s_hj) * ||v_j||_1) per head, and the final
+//                   I_j = sum_h 2^(t_hj - m_h) / l_h once m_h, l_h are known;
+//   Fig. 1 caption  one token is evicted after every attention call.
 //
-// One CTA = one chunk (up to 32 tiles of 64 slots) of one (b, kvh) unit.
+// Grid (nchunk, units). CTA (c, u) owns chunk c (up to 32 tiles of 64 slots)
+// of unit u = (b, kvh):
 //   warp 4, lane 0 : producer. TMA-loads the K and V tiles of the chunk's
-//                    live tiles (128-byte swizzled, 3-stage mbarrier ring,
-//                    L2 evict-first: every byte is read once per step).
+//                    live tiles (128-byte swizzled boxes, 3-stage mbarrier
+//                    ring, L2 evict-first: each byte is read once per step).
 //   warps 0..3     : consumers. Warp w owns rows 16w..16w+15 of every tile
 //                    and keeps its own online-softmax state. Per 16 slots:
 //        S^T[16 x 8]  = K[16 x D] . Q^T[D x 8]       (mma m16n8k16, heads as N)
@@ -23,6 +28,11 @@
 //   GQA folding: the g <= 8 query heads of the unit share each K/V byte.
 //   Masked slots are removed by select (logit -inf, V columns zeroed), so
 //   NaN or Inf in masked rows never reaches the output.
+// The CTA then publishes its chunk's (m, l, O) and counts itself in. The last
+// CTA of the unit merges the chunks, writes the output row, finishes
+// LongFlowScore for every live slot, reduces the lexicographic (I_j, j)
+// argmin over slots with age >= W and drops the unit's scratch lines from L2
+// without writing them back.
 #include <math.h>
 
 #include "../../include/lf_decode.h"
@@ -33,13 +43,14 @@ namespace lf {
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;
 constexpr int kStages = 3;
 constexpr uint32_t kOnesBf16x2 = 0x3F803F80u;   // (1.0, 1.0) in bf16
 constexpr uint32_t kAbsBf16x2 = 0x7FFF7FFFu;
 
 template <int D>
-struct SplitSmem {
+struct StepSmem {
     static constexpr int kBoxes = D / kBoxCols;
     static constexpr int kBoxBytes = kTile * 128;              // 64 rows x 128 B
     static constexpr int kTensorBytes = kBoxes * kBoxBytes;    // K (or V) of one tile
@@ -54,27 +65,163 @@ struct SplitSmem {
 };
 
 __device__ __forceinline__ void consumer_bar_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 }
 
 // Byte offset of 16-byte chunk `cg` (8 bf16 columns) of tile row `row` in a
 // swizzled K or V tile buffer.
 template <int D>
 __device__ __forceinline__ uint32_t swz_off(int row, int cg) {
-    return (cg >> 3) * SplitSmem<D>::kBoxBytes + row * 128 + (((cg & 7) ^ (row & 7)) << 4);
+    return (cg >> 3) * StepSmem<D>::kBoxBytes + row * 128 + (((cg & 7) ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ bool better(float v, int j, float bv, int bj) {
+    return v < bv || (v == bv && j < bj);
+}
+
+template <int G>
+__device__ __forceinline__ void load_terms(const float* t, float (&v)[G]) {
+    if constexpr (G == 1) {
+        v[0] = __ldcg(t);
+    } else if constexpr (G == 2) {
+        const float2 a = __ldcg(reinterpret_cast<const float2*>(t));
+        v[0] = a.x;
+        v[1] = a.y;
+    } else {
+#pragma unroll
+        for (int q = 0; q < G / 4; ++q) {
+            const float4 a = __ldcg(reinterpret_cast<const float4*>(t) + q);
+            v[4 * q] = a.x;
+            v[4 * q + 1] = a.y;
+            v[4 * q + 2] = a.z;
+            v[4 * q + 3] = a.w;
+        }
+    }
+}
+
+// Drops the 128-byte lines lying wholly inside [p, p + bytes).
+__device__ __forceinline__ void discard_range(const void* p, size_t bytes, int tid, int nthreads) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uintptr_t first = (a + 127) & ~static_cast<uintptr_t>(127);
+    const uintptr_t end = (a + bytes) & ~static_cast<uintptr_t>(127);
+    for (uintptr_t line = first + static_cast<uintptr_t>(tid) * 128; line < end;
+         line += static_cast<uintptr_t>(nthreads) * 128)
+        discard_l2_line(reinterpret_cast<const void*>(line));
+}
+
+// Merge of the unit's chunks by its last CTA (consumer threads only).
+template <int D, int G>
+__device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) {
+    const int nchunk = p.nchunk;
+    float* s_w = reinterpret_cast<float*>(smem);  // [nchunk][G]: 2^(m_c - m) / l
+    float* s_m = s_w + nchunk * G;                // [G]
+    float* s_il = s_m + G;                        // [G]
+    float* red_v = s_il + G;                      // [4]
+    int* red_j = reinterpret_cast<int*>(red_v + kConsumerWarps);
+    const float2* ml = p.part_ml + static_cast<size_t>(u) * nchunk * G;
+
+    if (tid < G) {
+        float m = -INFINITY;
+        for (int c = 0; c < nchunk; ++c) m = fmaxf(m, __ldcg(&ml[c * G + tid]).x);
+        float l = 0.f;
+        for (int c = 0; c < nchunk; ++c) {
+            const float2 v = __ldcg(&ml[c * G + tid]);
+            if (v.x != -INFINITY) l += v.y * exp2f(v.x - m);
+        }
+        s_m[tid] = m;
+        s_il[tid] = (l > 0.f) ? 1.f / l : 0.f;
+    }
+    consumer_bar_sync();
+    for (int e = tid; e < nchunk * G; e += kConsumers) {
+        const float2 v = __ldcg(&ml[e]);
+        const int h = e % G;
+        s_w[e] = (v.x == -INFINITY) ? 0.f : exp2f(v.x - s_m[h]) * s_il[h];
+    }
+    consumer_bar_sync();
+
+    // Output: O_h = sum_c w_ch * O_ch, rounded to bf16.
+    const int b = u / p.Hkv;
+    const int kvh = u - b * p.Hkv;
+    const float* po = p.part_o + static_cast<size_t>(u) * nchunk * G * D;
+    __nv_bfloat16* out = p.out + (static_cast<size_t>(b) * p.Hq + kvh * G) * D;
+    for (int e = tid; e < G * D; e += kConsumers) {
+        const int h = e / D;
+        float o = 0.f;
+        for (int c = 0; c < nchunk; ++c) {
+            const float w = s_w[c * G + h];
+            if (w != 0.f) o += w * __ldcg(&po[static_cast<size_t>(c) * G * D + e]);
+        }
+        out[e] = __float2bfloat16_rn(o);
+    }
+
+    // LongFlowScore of every live slot; argmin over the eligible ones.
+    float m[G], il[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m[h] = s_m[h];
+        il[h] = s_il[h];
+    }
+    const int S = p.S;
+    const int32_t* age = p.mask + static_cast<size_t>(u) * S;
+    const float* stash = p.stash + static_cast<size_t>(u) * S * G;
+    float* scores = p.scores ? p.scores + static_cast<size_t>(u) * S : nullptr;
+    float best = INFINITY;
+    int bestj = 0x7fffffff;
+    for (int j = tid; j < S; j += kConsumers) {
+        const int a = __ldcg(&age[j]);
+        float I = INFINITY;
+        if (a >= 0) {
+            float t[G];
+            load_terms<G>(stash + static_cast<size_t>(j) * G, t);
+            I = 0.f;
+#pragma unroll
+            for (int h = 0; h < G; ++h) I += exp2f(t[h] - m[h]) * il[h];
+            if (a >= p.W && better(I, j, best, bestj)) {
+                best = I;
+                bestj = j;
+            }
+        }
+        if (scores) scores[j] = I;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, off);
+        const int oj = __shfl_xor_sync(0xffffffffu, bestj, off);
+        if (better(ov, oj, best, bestj)) {
+            best = ov;
+            bestj = oj;
+        }
+    }
+    if ((tid & 31) == 0) {
+        red_v[tid >> 5] = best;
+        red_j[tid >> 5] = bestj;
+    }
+    consumer_bar_sync();
+    if (tid == 0) {
+        for (int w = 1; w < kConsumerWarps; ++w)
+            if (better(red_v[w], red_j[w], best, bestj)) {
+                best = red_v[w];
+                bestj = red_j[w];
+            }
+        p.next_slot[u] = (bestj == 0x7fffffff) ? -1 : bestj;
+    }
+    // Every read of the unit's scratch is done: drop the lines, no write-back.
+    discard_range(stash, static_cast<size_t>(S) * G * sizeof(float), tid, kConsumers);
+    discard_range(po, static_cast<size_t>(nchunk) * G * D * sizeof(float), tid, kConsumers);
 }
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 2)
-    lf_attn_split_kernel(const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
-    using L = SplitSmem<D>;
+    lf_decode_step_kernel(const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const StepParams p) {
+    using L = StepSmem<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     int32_t* ages = reinterpret_cast<int32_t*>(smem + L::kAgesOff);
     int32_t* list = reinterpret_cast<int32_t*>(smem + L::kListOff);
-    volatile int32_t* misc = reinterpret_cast<int32_t*>(smem + L::kMiscOff);  // [0] count, [1] abort
+    // [0] live tile count, [1] abort flag, [2] last-CTA flag
+    volatile int32_t* misc = reinterpret_cast<int32_t*>(smem + L::kMiscOff);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
     uint64_t* empty = full + kStages;
 
@@ -117,10 +264,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         ages[i] = a;
     }
+    __threadfence();  // the aged mask is read by the unit's last CTA
     __syncthreads();
 
     // Tiles with no live slot are never loaded (ragged fills stream only
-    // their live prefix).
+    // their live part).
     if (warp == 0) {
         int cnt = 0;
         for (int t = 0; t < ntiles; ++t) {
@@ -258,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float x2 = (liveB && hv0) ? sc[2] * sl : NEG;
         const float x3 = (liveB && hv1) ? sc[3] * sl : NEG;
 
-        // Per-slot score terms: log2(exp(s) * ||v||_1), rebased by the combine.
+        // Per-slot score terms t = log2(exp(s) * ||v||_1).
         if (hv0) {
             const int slotA = tslot0 + wrow0 + r;
             float* st = p.stash + (static_cast<size_t>(u) * S + slotA) * G + h0;
@@ -333,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    // ------------------------------------------------ merge the 4 warps --
+    // ------------------------------------------ merge the 4 warps' state --
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
@@ -364,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const size_t pidx = static_cast<size_t>(u) * p.nchunk + chunk;
     if (cnt > 0) {
         float* po = p.part_o + pidx * G * D;
-        for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
+        for (int e = tid; e < G * D; e += kConsumers) {
             const int h = e / D;
             float mh = NEG;
 #pragma unroll
@@ -380,54 +528,68 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (tid < G) {
         float mh = NEG;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) mh = fmaxf(mh, wm[w * G + tid]);
         float l = 0.f;
         if (cnt > 0) {
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) mh = fmaxf(mh, wm[w * G + tid]);
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
                 const float mw = wm[w * G + tid];
                 if (mw != NEG) l += wl[w * G + tid] * exp2f(mw - mh);
             }
-        } else {
-            mh = NEG;
         }
         p.part_ml[pidx * G + tid] = make_float2(mh, l);
     }
+
+    // ---------------------------------------- last CTA of the unit merges --
+    __threadfence();
+    consumer_bar_sync();
+    if (tid == 0) {
+        int last = 1;
+        if (p.nchunk > 1) {
+            const uint32_t prev = atomicAdd(&p.arrivals[u], 1u);
+            last = (prev == static_cast<uint32_t>(p.nchunk - 1));
+            if (last) p.arrivals[u] = 0u;  // every chunk of the unit has arrived
+        }
+        misc[2] = last;
+    }
+    consumer_bar_sync();
+    if (!misc[2]) return;
+    __threadfence();
+    finish_unit<D, G>(p, u, smem, tid);
 }
 
 template <int D, int G>
-cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
-                           int units, cudaStream_t stream) {
+cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
+                     int units, cudaStream_t stream) {
     static int configured_for = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_for != dev) {
-        e = cudaFuncSetAttribute(lf_attn_split_kernel<D, G>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SplitSmem<D>::kAlloc);
+        e = cudaFuncSetAttribute(lf_decode_step_kernel<D, G>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, StepSmem<D>::kAlloc);
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
     dim3 grid(p.nchunk, units);
-    lf_attn_split_kernel<D, G><<<grid, kThreads, SplitSmem<D>::kAlloc, stream>>>(tmK, tmV, p);
+    lf_decode_step_kernel<D, G><<<grid, kThreads, StepSmem<D>::kAlloc, stream>>>(tmK, tmV, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t split_smem_bytes(int D) {
-    return D == 64 ? SplitSmem<64>::kAlloc : SplitSmem<128>::kAlloc;
+size_t step_smem_bytes(int D) {
+    return D == 64 ? StepSmem<64>::kAlloc : StepSmem<128>::kAlloc;
 }
 
-cudaError_t launch_attn_split(int D, int G, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                              const SplitParams& p, int units, cudaStream_t stream) {
-#define LF_SPLIT_CASE(DD, GG) \
-    if (D == DD && G == GG) return launch_split_t<DD, GG>(tmK, tmV, p, units, stream);
-    LF_SPLIT_CASE(64, 1) LF_SPLIT_CASE(64, 2) LF_SPLIT_CASE(64, 4) LF_SPLIT_CASE(64, 8)
-    LF_SPLIT_CASE(128, 1) LF_SPLIT_CASE(128, 2) LF_SPLIT_CASE(128, 4) LF_SPLIT_CASE(128, 8)
-#undef LF_SPLIT_CASE
+cudaError_t launch_decode_step(int D, int G, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                               const StepParams& p, int units, cudaStream_t stream) {
+#define LF_STEP_CASE(DD, GG) \
+    if (D == DD && G == GG) return launch_t<DD, GG>(tmK, tmV, p, units, stream);
+    LF_STEP_CASE(64, 1) LF_STEP_CASE(64, 2) LF_STEP_CASE(64, 4) LF_STEP_CASE(64, 8)
+    LF_STEP_CASE(128, 1) LF_STEP_CASE(128, 2) LF_STEP_CASE(128, 4) LF_STEP_CASE(128, 8)
+#undef LF_STEP_CASE
     return cudaErrorInvalidValue;
 }
 

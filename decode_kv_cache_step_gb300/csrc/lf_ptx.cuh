@@ -93,6 +93,12 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// Drops a 128-byte L2 line of scratch without writing it back to DRAM. The
+// line's contents become undefined; use only on data nobody reads again.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // ------------------------------------------------------- warp MMA fragments --
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {

@@ -73,10 +73,9 @@ typedef enum lf_status {
 #define LF_DEVERR_BAD_WRITE_SLOT 0x1u /* a write_slot outside [-1, S) was ignored */
 #define LF_DEVERR_WAIT_TIMEOUT 0x2u   /* a pipeline wait gave up; that step's results are invalid */
 
-/* Kernel ids for lf_profile_collect. */
-#define LF_KERNEL_ATTN_SPLIT 0 /* slot write + mask ageing + split attention + score terms */
-#define LF_KERNEL_COMBINE 1    /* split merge + output + LongFlowScore + argmin */
-#define LF_KERNEL_COUNT 2
+/* Kernel ids for lf_profile_collect. A decode step is one launch of one kernel. */
+#define LF_KERNEL_DECODE_STEP 0 /* slot write, mask ageing, attention, score, argmin */
+#define LF_KERNEL_COUNT 1
 
 /*
  * One decode step (all three stages above) on device buffers.

@@ -92,7 +92,7 @@ def test_scores_and_host_variants_validate_too(lib):
 
 def test_profile_api_without_launches(lib):
     lf.profile_enable(True)
-    assert lf.profile_collect(lf.LF_KERNEL_ATTN_SPLIT) == (0.0, 0)
+    assert lf.profile_collect(lf.LF_KERNEL_DECODE_STEP) == (0.0, 0)
     lf.profile_enable(False)
     with pytest.raises(lf.LFError):
         lf.profile_collect(7)

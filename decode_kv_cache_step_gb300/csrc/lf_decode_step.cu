@@ -167,21 +167,38 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) 
     float* scores = p.scores ? p.scores + static_cast<size_t>(u) * S : nullptr;
     float best = INFINITY;
     int bestj = 0x7fffffff;
-    for (int j = tid; j < S; j += kConsumers) {
-        const int a = __ldcg(&age[j]);
-        float I = INFINITY;
-        if (a >= 0) {
-            float t[G];
-            load_terms<G>(stash + static_cast<size_t>(j) * G, t);
-            I = 0.f;
+    // Batches of kBatch slots per thread: all loads of a batch are in flight
+    // together instead of one L2 round trip per slot.
+    constexpr int kBatch = 8;
+    for (int j0 = tid; j0 < S; j0 += kBatch * kConsumers) {
+        int a[kBatch];
+        float t[kBatch][G];
 #pragma unroll
-            for (int h = 0; h < G; ++h) I += exp2f(t[h] - m[h]) * il[h];
-            if (a >= p.W && better(I, j, best, bestj)) {
-                best = I;
-                bestj = j;
-            }
+        for (int k = 0; k < kBatch; ++k) {
+            const int j = j0 + k * kConsumers;
+            a[k] = (j < S) ? __ldcg(&age[j]) : -1;
         }
-        if (scores) scores[j] = I;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int j = j0 + k * kConsumers;
+            if (j < S) load_terms<G>(stash + static_cast<size_t>(j) * G, t[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int j = j0 + k * kConsumers;
+            if (j >= S) break;
+            float I = INFINITY;
+            if (a[k] >= 0) {
+                I = 0.f;
+#pragma unroll
+                for (int h = 0; h < G; ++h) I += exp2f(t[k][h] - m[h]) * il[h];
+                if (a[k] >= p.W && better(I, j, best, bestj)) {
+                    best = I;
+                    bestj = j;
+                }
+            }
+            if (scores) scores[j] = I;
+        }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -251,18 +268,48 @@ __global__ void __launch_bounds__(kThreads, 2)
         fence_barrier_init();
     }
 
-    // Slot write, part 1 (Fig. 2 Left): age the chunk's mask. The written slot
-    // gets age 0 (and becomes live); other live slots age by one.
-    int32_t* mrow = p.mask + static_cast<size_t>(u) * S;
-    for (int i = tid; i < n; i += kThreads) {
-        const int j = slot0 + i;
-        int a = mrow[j];
-        if (ws >= 0) {
-            const int na = (j == ws) ? 0 : ((a >= 0 && a != 0x7fffffff) ? a + 1 : a);
-            if (na != a) mrow[j] = na;
-            a = na;
+    // Q^T as the B operand of S^T = K . Q^T, loaded early so its latency
+    // overlaps the mask prologue: b0 = (d = 16kk + h0 .. +1, head r), b1 = d + 8.
+    const int b = u / p.Hkv;
+    const int kvh = u - b * p.Hkv;
+    const int r = lane >> 2;          // fragment row (slot) 0..7
+    const int h0 = 2 * (lane & 3);    // fragment columns (heads) h0, h0+1
+    uint32_t qf[D / 16][2];
+    if (warp < kConsumerWarps) {
+        const bool valid = r < G;
+        const __nv_bfloat16* qrow =
+            p.q + (static_cast<size_t>(b) * p.Hq + kvh * G + (valid ? r : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int dc = kk * 16 + h0;
+            qf[kk][0] = valid ? *reinterpret_cast<const uint32_t*>(qrow + dc) : 0u;
+            qf[kk][1] = valid ? *reinterpret_cast<const uint32_t*>(qrow + dc + 8) : 0u;
         }
-        ages[i] = a;
+    }
+
+    // Slot write, part 1 (Fig. 2 Left): age the chunk's mask. The written slot
+    // gets age 0 (and becomes live); other live slots age by one. Every load
+    // is issued before any store, so the chunk's mask costs one round trip.
+    constexpr int kPer = (kMaxChunkTiles * kTile + kThreads - 1) / kThreads;
+    int32_t* mrow = p.mask + static_cast<size_t>(u) * S + slot0;
+    int av[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int i = tid + k * kThreads;
+        av[k] = (i < n) ? mrow[i] : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int i = tid + k * kThreads;
+        if (i < n) {
+            int a = av[k];
+            if (ws >= 0) {
+                const int na = (slot0 + i == ws) ? 0 : ((a >= 0 && a != 0x7fffffff) ? a + 1 : a);
+                if (na != a) mrow[i] = na;
+                a = na;
+            }
+            ages[i] = a;
+        }
     }
     __threadfence();  // the aged mask is read by the unit's last CTA
     __syncthreads();
@@ -317,27 +364,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // --------------------------------------------------------- consumers --
-    const int b = u / p.Hkv;
-    const int kvh = u - b * p.Hkv;
-    const int r = lane >> 2;          // fragment row (slot) 0..7
-    const int h0 = 2 * (lane & 3);    // fragment columns (heads) h0, h0+1
     const bool hv0 = h0 < G;
     const bool hv1 = h0 + 1 < G;
     const float NEG = -INFINITY;
-
-    // Q^T as the B operand: b0 = (d = 16kk + h0 .. +1, head r), b1 = d + 8.
-    uint32_t qf[D / 16][2];
-    {
-        const bool valid = r < G;
-        const __nv_bfloat16* qrow =
-            p.q + (static_cast<size_t>(b) * p.Hq + kvh * G + (valid ? r : 0)) * D;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const int dc = kk * 16 + h0;
-            qf[kk][0] = valid ? *reinterpret_cast<const uint32_t*>(qrow + dc) : 0u;
-            qf[kk][1] = valid ? *reinterpret_cast<const uint32_t*>(qrow + dc + 8) : 0u;
-        }
-    }
 
     float acc[D / 16][4];
 #pragma unroll

@@ -188,12 +188,15 @@ lf_status encode_cache_map(CUtensorMap* m, void* base, int D, int S, int units) 
 // ---------------------------------------------------------------- planning --
 
 struct Plan {
-    int tiles, chunk_tiles, nchunk;
+    int tiles, chunk_tiles, nchunk, stages;
 };
 
-// Split the slot axis of every unit into nchunk chunks of chunk_tiles tiles:
-// enough CTAs to fill the GPU several times over, chunks as long as
-// possible, at most kMaxChunkTiles tiles and kMaxNChunk chunks.
+// Split the slot axis of every unit into nchunk chunks of chunk_tiles tiles.
+// Each CTA costs a fixed start-up and merge, so chunks stay long (13 to 32
+// tiles) as long as the grid still has about 3000 CTAs, about 20 per SM, to
+// balance the tail; a batch too small to fill the GPU that way uses short
+// chunks of about 5 tiles instead. At most kMaxChunkTiles tiles and
+// kMaxNChunk chunks.
 Plan plan_split(int S, int units, int sms) {
     Plan pl;
     pl.tiles = (S + lf::kTile - 1) / lf::kTile;
@@ -203,13 +206,19 @@ Plan plan_split(int S, int units, int sms) {
         if (ct >= 1 && ct <= lf::kMaxChunkTiles) nchunk = (pl.tiles + ct - 1) / ct;
     }
     if (nchunk == 0) {
-        const long target_ctas = 8L * sms;
-        nchunk = static_cast<int>((target_ctas + units - 1) / units);
+        const int longest = (pl.tiles + lf::kMaxChunkTiles - 1) / lf::kMaxChunkTiles;
+        const int fill = static_cast<int>((20L * sms + units - 1) / units);
+        if (static_cast<long>(units) * longest >= sms)
+            nchunk = std::max(longest, std::min(fill, (pl.tiles + 12) / 13));
+        else
+            nchunk = (pl.tiles + 4) / 5;
     }
     nchunk = std::max(nchunk, (pl.tiles + lf::kMaxChunkTiles - 1) / lf::kMaxChunkTiles);
     nchunk = std::min(std::max(nchunk, 1), std::min(pl.tiles, kMaxNChunk));
     pl.chunk_tiles = (pl.tiles + nchunk - 1) / nchunk;
     pl.nchunk = (pl.tiles + pl.chunk_tiles - 1) / pl.chunk_tiles;
+    pl.stages = 2;
+    if (const char* env = std::getenv("LF_STAGES")) pl.stages = (std::atoi(env) == 3) ? 3 : 2;
     return pl;
 }
 
@@ -323,7 +332,7 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
     cudaError_t e;
     {
         ProfScope prof(LF_KERNEL_DECODE_STEP, stream);
-        e = lf::launch_decode_step(s.d, g, tmK, tmV, sp, units, stream);
+        e = lf::launch_decode_step(s.d, g, pl.stages, tmK, tmV, sp, units, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");
     return LF_OK;

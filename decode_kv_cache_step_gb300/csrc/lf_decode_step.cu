@@ -45,11 +45,10 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
-constexpr int kStages = 3;
 constexpr uint32_t kOnesBf16x2 = 0x3F803F80u;   // (1.0, 1.0) in bf16
 constexpr uint32_t kAbsBf16x2 = 0x7FFF7FFFu;
 
-template <int D>
+template <int D, int kStages>
 struct StepSmem {
     static constexpr int kBoxes = D / kBoxCols;
     static constexpr int kBoxBytes = kTile * 128;              // 64 rows x 128 B
@@ -70,9 +69,10 @@ __device__ __forceinline__ void consumer_bar_sync() {
 
 // Byte offset of 16-byte chunk `cg` (8 bf16 columns) of tile row `row` in a
 // swizzled K or V tile buffer.
-template <int D>
+constexpr int kBoxBytes = kTile * 128;  // one 64-row x 128-byte swizzled box
+
 __device__ __forceinline__ uint32_t swz_off(int row, int cg) {
-    return (cg >> 3) * StepSmem<D>::kBoxBytes + row * 128 + (((cg & 7) ^ (row & 7)) << 4);
+    return (cg >> 3) * kBoxBytes + row * 128 + (((cg & 7) ^ (row & 7)) << 4);
 }
 
 __device__ __forceinline__ bool better(float v, int j, float bv, int bj) {
@@ -144,14 +144,39 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) 
     const int kvh = u - b * p.Hkv;
     const float* po = p.part_o + static_cast<size_t>(u) * nchunk * G * D;
     __nv_bfloat16* out = p.out + (static_cast<size_t>(b) * p.Hq + kvh * G) * D;
-    for (int e = tid; e < G * D; e += kConsumers) {
-        const int h = e / D;
-        float o = 0.f;
-        for (int c = 0; c < nchunk; ++c) {
-            const float w = s_w[c * G + h];
-            if (w != 0.f) o += w * __ldcg(&po[static_cast<size_t>(c) * G * D + e]);
+    // Loads of four chunks are issued together; a chunk that had no live
+    // tile has weight 0 and its (unwritten) partial is selected away.
+    constexpr int kPerT = (G * D + kConsumers - 1) / kConsumers;
+    float o[kPerT];
+#pragma unroll
+    for (int k = 0; k < kPerT; ++k) o[k] = 0.f;
+    for (int c0 = 0; c0 < nchunk; c0 += 4) {
+        float v[4][kPerT];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const int c = min(c0 + cc, nchunk - 1);
+#pragma unroll
+            for (int k = 0; k < kPerT; ++k) {
+                const int e = tid + k * kConsumers;
+                v[cc][k] = (e < G * D) ? __ldcg(&po[static_cast<size_t>(c) * G * D + e]) : 0.f;
+            }
         }
-        out[e] = __float2bfloat16_rn(o);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const int c = c0 + cc;
+            if (c >= nchunk) break;
+#pragma unroll
+            for (int k = 0; k < kPerT; ++k) {
+                const int e = tid + k * kConsumers;
+                const float w = (e < G * D) ? s_w[c * G + e / D] : 0.f;
+                o[k] += (w != 0.f) ? w * v[cc][k] : 0.f;
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kPerT; ++k) {
+        const int e = tid + k * kConsumers;
+        if (e < G * D) out[e] = __float2bfloat16_rn(o[k]);
     }
 
     // LongFlowScore of every live slot; argmin over the eligible ones.
@@ -227,11 +252,12 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) 
     discard_range(po, static_cast<size_t>(nchunk) * G * D * sizeof(float), tid, kConsumers);
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 2)
+// kStages-deep TMA ring; 3 stages run 2 CTAs per SM, 2 stages run 3.
+template <int D, int G, int kStages>
+__global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
     lf_decode_step_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const StepParams p) {
-    using L = StepSmem<D>;
+    using L = StepSmem<D, kStages>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -395,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (cg < D / 8) {
                 const __nv_bfloat16* src = (is_v ? p.new_v : p.new_k) + static_cast<size_t>(u) * D;
                 const uint4 val = reinterpret_cast<const uint4*>(src)[cg];
-                *reinterpret_cast<uint4*>((is_v ? vb : kb) + swz_off<D>(row, cg)) = val;
+                *reinterpret_cast<uint4*>((is_v ? vb : kb) + swz_off(row, cg)) = val;
                 __nv_bfloat16* dst =
                     (is_v ? p.v_cache : p.k_cache) + (static_cast<size_t>(u) * S + ws) * D;
                 reinterpret_cast<uint4*>(dst)[cg] = val;
@@ -418,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint32_t vbase = smem_u32(vb);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = swz_off<D>(lrow, 2 * kk + (lane >> 4));
+                const uint32_t off = swz_off(lrow, 2 * kk + (lane >> 4));
                 uint32_t a[4], v[4];
                 ldsm_x4(kbase + off, a);
                 ldsm_x4(vbase + off, v);
@@ -498,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
                 uint32_t a[4];
-                ldsm_x4_trans(vbase + swz_off<D>(lrow, 2 * mt + ((lane >> 3) & 1)), a);
+                ldsm_x4_trans(vbase + swz_off(lrow, 2 * mt + ((lane >> 3) & 1)), a);
                 a[0] &= mlo;
                 a[1] &= mlo;
                 a[2] &= mhi;
@@ -588,34 +614,44 @@ __global__ void __launch_bounds__(kThreads, 2)
     finish_unit<D, G>(p, u, smem, tid);
 }
 
-template <int D, int G>
+template <int D, int G, int kStages>
 cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
                      int units, cudaStream_t stream) {
+    using L = StepSmem<D, kStages>;
     static int configured_for = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_for != dev) {
-        e = cudaFuncSetAttribute(lf_decode_step_kernel<D, G>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, StepSmem<D>::kAlloc);
+        e = cudaFuncSetAttribute(lf_decode_step_kernel<D, G, kStages>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
     dim3 grid(p.nchunk, units);
-    lf_decode_step_kernel<D, G><<<grid, kThreads, StepSmem<D>::kAlloc, stream>>>(tmK, tmV, p);
+    lf_decode_step_kernel<D, G, kStages><<<grid, kThreads, L::kAlloc, stream>>>(tmK, tmV, p);
     return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t launch_dg(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
+                      int units, cudaStream_t stream, int stages) {
+    return stages == 2 ? launch_t<D, G, 2>(tmK, tmV, p, units, stream)
+                       : launch_t<D, G, 3>(tmK, tmV, p, units, stream);
 }
 
 }  // namespace
 
-size_t step_smem_bytes(int D) {
-    return D == 64 ? StepSmem<64>::kAlloc : StepSmem<128>::kAlloc;
+size_t step_smem_bytes(int D, int stages) {
+    if (stages == 2) return D == 64 ? StepSmem<64, 2>::kAlloc : StepSmem<128, 2>::kAlloc;
+    return D == 64 ? StepSmem<64, 3>::kAlloc : StepSmem<128, 3>::kAlloc;
 }
 
-cudaError_t launch_decode_step(int D, int G, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                               const StepParams& p, int units, cudaStream_t stream) {
+cudaError_t launch_decode_step(int D, int G, int stages, const CUtensorMap& tmK,
+                               const CUtensorMap& tmV, const StepParams& p, int units,
+                               cudaStream_t stream) {
 #define LF_STEP_CASE(DD, GG) \
-    if (D == DD && G == GG) return launch_t<DD, GG>(tmK, tmV, p, units, stream);
+    if (D == DD && G == GG) return launch_dg<DD, GG>(tmK, tmV, p, units, stream, stages);
     LF_STEP_CASE(64, 1) LF_STEP_CASE(64, 2) LF_STEP_CASE(64, 4) LF_STEP_CASE(64, 8)
     LF_STEP_CASE(128, 1) LF_STEP_CASE(128, 2) LF_STEP_CASE(128, 4) LF_STEP_CASE(128, 8)
 #undef LF_STEP_CASE

@@ -37,10 +37,12 @@ struct StepParams {
     float scale_log2;            // scale * log2(e)
 };
 
-// Dynamic shared memory the kernel needs for head dim D.
-size_t step_smem_bytes(int D);
+// Dynamic shared memory the kernel needs for head dim D and a TMA ring of
+// `stages` tiles (2 or 3).
+size_t step_smem_bytes(int D, int stages);
 
-cudaError_t launch_decode_step(int D, int G, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                               const StepParams& p, int units, cudaStream_t stream);
+cudaError_t launch_decode_step(int D, int G, int stages, const CUtensorMap& tmK,
+                               const CUtensorMap& tmV, const StepParams& p, int units,
+                               cudaStream_t stream);
 
 }  // namespace lf

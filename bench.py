@@ -256,14 +256,16 @@ def bench_lf(args, wl):
     lf.load_library()
 
     # Each rank runs its own B sequences of the recipe (weak scaling).
-    host = initial_state(wl, batch_offset=rank * wl.B)
+    from decode_kv_cache_step_gb300.sharding import max_over_ranks, weak_shard
+    shard = weak_shard(wl, rank, world)
+    host = initial_state(wl, batch_offset=shard.batch_offset)
     lengths = host["lengths"]
     k = bf16_dev(host["k_cache"], device)
     v = bf16_dev(host["v_cache"], device)
     mask = torch.from_numpy(host["mask"]).to(device)
     pool = []
     for s in range(8):
-        inp = step_inputs(wl, s, batch_offset=rank * wl.B, full_batch=wl.B * world)
+        inp = step_inputs(wl, s, batch_offset=shard.batch_offset, full_batch=shard.full_batch)
         pool.append({kk: bf16_dev(vv, device) for kk, vv in inp.items()})
     out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.bfloat16, device=device)
     slots = [torch.full((wl.B, wl.Hkv), -1, dtype=torch.int32, device=device),
@@ -301,10 +303,7 @@ def bench_lf(args, wl):
     lf.profile_enable(False)
     ms_total = ev0.elapsed_time(ev1)
     kern_ms, kern_n = lf.profile_collect(lf.LF_KERNEL_DECODE_STEP)
-    if world > 1:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, device)
     if lf.device_errors(stream) != 0:
         raise RuntimeError("device error word set during the timed steps")
 
@@ -312,7 +311,7 @@ def bench_lf(args, wl):
     pin = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
     hpool = []
     for s in range(8):
-        inp = step_inputs(wl, s, batch_offset=rank * wl.B, full_batch=wl.B * world)
+        inp = step_inputs(wl, s, batch_offset=shard.batch_offset, full_batch=shard.full_batch)
         hpool.append({kk: pin(vv).view(torch.bfloat16) for kk, vv in inp.items()})
     h_out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.bfloat16).pin_memory()
     h_ws = torch.full((wl.B, wl.Hkv), -1, dtype=torch.int32).pin_memory()
@@ -333,10 +332,7 @@ def bench_lf(args, wl):
     for i in range(args.steps):
         e2e_step(i)
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, device)
     clocks.stop()
     h2d = (wl.B * wl.Hq * wl.d * 2) + 2 * (wl.B * wl.Hkv * wl.d * 2) + wl.B * wl.Hkv * 4
     d2h = wl.B * wl.Hq * wl.d * 2 + wl.B * wl.Hkv * 4

@@ -30,7 +30,8 @@ KERNEL_NAMES = {LF_KERNEL_DECODE_STEP: "lf_decode_step_kernel"}
 
 # Every exported symbol of include/lf_decode.h.
 EXPORTED = (
-    "lf_decode_step", "lf_decode_step_scores", "lf_decode_step_host", "lf_device_errors",
+    "lf_decode_step", "lf_decode_step_scores", "lf_decode_step_host", "lf_decode_step_noalloc",
+    "lf_device_errors",
     "lf_profile_enable", "lf_profile_collect", "lf_release_workspace", "lf_status_string",
     "lf_last_error", "lf_version",
 )
@@ -68,6 +69,8 @@ def load_library(path: str | None = None):
         step_args = [P] * 9 + [I] * 6 + [F, P]
         lib.lf_decode_step.argtypes = step_args
         lib.lf_decode_step_host.argtypes = step_args
+        lib.lf_decode_step_noalloc.argtypes = step_args
+        lib.lf_decode_step_noalloc.restype = I
         lib.lf_decode_step_scores.argtypes = [P] * 10 + [I] * 6 + [F, P]
         for fn in (lib.lf_decode_step, lib.lf_decode_step_host, lib.lf_decode_step_scores):
             fn.restype = I
@@ -178,6 +181,20 @@ def decode_step_host(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, n
     B, Hq, Hkv, d, S = _check_step(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out,
                                    next_slot, io_on_device=False)
     _check(lib, lib.lf_decode_step_host(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), mask.data_ptr(), new_k.data_ptr(),
+        new_v.data_ptr(), write_slot.data_ptr(), out.data_ptr(), next_slot.data_ptr(),
+        B, Hq, Hkv, d, S, int(W), float(scale), _stream_handle(stream)))
+
+
+def decode_step_noalloc(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slot, W,
+                        scale, stream=None):
+    """lf_decode_step_noalloc: lf_decode_step with the library's fixed 16 MiB
+    scratch instead of cudaMalloc, for callers that cannot allocate device
+    memory. Calls that overlap on the GPU share that scratch and race."""
+    lib = load_library()
+    B, Hq, Hkv, d, S = _check_step(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out,
+                                   next_slot)
+    _check(lib, lib.lf_decode_step_noalloc(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), mask.data_ptr(), new_k.data_ptr(),
         new_v.data_ptr(), write_slot.data_ptr(), out.data_ptr(), next_slot.data_ptr(),
         B, Hq, Hkv, d, S, int(W), float(scale), _stream_handle(stream)))

@@ -353,6 +353,34 @@ lf_status run_step(const StepArgs& a, const Shape& s, void* stream_v) {
     return enqueue_step(a, s, stream, scr, L, pl);
 }
 
+// ------------------------------------------------- static scratch variant --
+//
+// lf_decode_step_noalloc runs the same decode-step kernel with its scratch
+// (softmax partials, per-slot score terms, arrival counters, error word) in
+// this fixed device array instead of memory from cudaMalloc. Every device that
+// loads this library holds the array until the process exits. In host code
+// the name is only a stand-in for the symbol: its device address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_base[kMaxDevices] = {};
+
+lf_status static_scratch_base(int dev, void** out) {
+    if (dev < 0 || dev >= kMaxDevices) return fail(LF_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_base[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        g_static_base[dev] = p;
+    }
+    *out = g_static_base[dev];
+    return LF_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -419,6 +447,71 @@ lf_status lf_decode_step_host(const void* q_host, void* k_cache, void* v_cache, 
     if ((e = cudaMemcpyAsync(out_host, stg + off_o, q_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
         (e = cudaMemcpyAsync(next_slot_host, stg + off_n, i_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
         return cuda_fail(e, "device-to-host copy");
+    return LF_OK;
+}
+
+lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, int32_t* mask,
+                                 const void* new_k, const void* new_v, const int32_t* write_slot,
+                                 void* out, int32_t* next_slot, int B, int Hq, int Hkv, int d,
+                                 int S, int W, float scale, void* stream_v) {
+    const StepArgs a{q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slot, nullptr};
+    const Shape s{B, Hq, Hkv, d, S, W, scale};
+    lf_status st = check_args(a, s);
+    if (st != LF_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    const size_t units = static_cast<size_t>(B) * Hkv;
+    const Plan pl = plan_split(S, static_cast<int>(units), sms > 0 ? sms : 1);
+    const Layout L = scratch_layout(s, pl, 0);
+    const size_t arrivals_off = align_up(L.total, 256);
+    const size_t err_off = align_up(arrivals_off + units * sizeof(uint32_t), 256);
+    const size_t need = err_off + 256;
+    if (need > kStaticScratchBytes)
+        return fail(LF_ERR_UNSUPPORTED,
+                    "lf_decode_step_noalloc: this shape needs %zu bytes of scratch but the static "
+                    "scratch holds %zu; use lf_decode_step or fewer B * Hkv * S slots",
+                    need, kStaticScratchBytes);
+    void* base_v = nullptr;
+    if ((st = static_scratch_base(dev, &base_v)) != LF_OK) return st;
+    char* base = static_cast<char*>(base_v);
+    // The arrival counters and the error word must start at zero.
+    if ((e = cudaMemsetAsync(base + arrivals_off, 0, need - arrivals_off, stream)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync(static scratch)");
+
+    const int g = Hq / Hkv;
+    CUtensorMap tmK, tmV;
+    if ((st = encode_cache_map(&tmK, k_cache, d, S, static_cast<int>(units))) != LF_OK) return st;
+    if ((st = encode_cache_map(&tmV, v_cache, d, S, static_cast<int>(units))) != LF_OK) return st;
+    lf::StepParams sp;
+    sp.q = static_cast<const __nv_bfloat16*>(q);
+    sp.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+    sp.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+    sp.mask = mask;
+    sp.new_k = static_cast<const __nv_bfloat16*>(new_k);
+    sp.new_v = static_cast<const __nv_bfloat16*>(new_v);
+    sp.write_slot = write_slot;
+    sp.out = static_cast<__nv_bfloat16*>(out);
+    sp.next_slot = next_slot;
+    sp.scores = nullptr;
+    sp.part_o = reinterpret_cast<float*>(base + L.o);
+    sp.part_ml = reinterpret_cast<float2*>(base + L.ml);
+    sp.stash = reinterpret_cast<float*>(base + L.stash);
+    sp.arrivals = reinterpret_cast<uint32_t*>(base + arrivals_off);
+    sp.dev_err = reinterpret_cast<uint32_t*>(base + err_off);
+    sp.Hq = Hq;
+    sp.Hkv = Hkv;
+    sp.S = S;
+    sp.W = W;
+    sp.nchunk = pl.nchunk;
+    sp.chunk_tiles = pl.chunk_tiles;
+    sp.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    g_last_error[0] = '\0';
+    e = lf::launch_decode_step(d, g, pl.stages, tmK, tmV, sp, static_cast<int>(units), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");
     return LF_OK;
 }
 

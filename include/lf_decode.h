@@ -125,6 +125,36 @@ lf_status lf_decode_step_host(const void* q_host, void* k_cache, void* v_cache, 
                               int W, float scale, void* stream);
 
 /*
+ * lf_decode_step for callers that cannot allocate device memory. The paper has
+ * no counterpart; this entry point exists for embedding. A serving engine that
+ * reserves all free GPU memory for its own pools at start-up has nothing left
+ * for cudaMalloc (and a real-time loop may not accept the device-wide
+ * synchronisation cudaMalloc and cudaFree can cause), yet lf_decode_step needs
+ * scratch and grows it on demand. This variant instead uses a fixed 16 MiB
+ * scratch array compiled into the library: it calls no cudaMalloc, cudaFree or
+ * other allocating routine. Same arguments, semantics and results as
+ * lf_decode_step.
+ *   - Limit: the shape's scratch (softmax partials, per-slot score terms of
+ *     B * Hkv * S slots in fp32 per query head, counters) must fit in 16 MiB,
+ *     roughly B * Hq * S <= 3 million for d = 128; larger shapes return
+ *     LF_ERR_UNSUPPORTED with the bytes needed.
+ *   - Every device that loads the library holds the 16 MiB until exit.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array; calls whose work overlaps on
+ *     the GPU (other streams, other host threads) race and corrupt each other.
+ *     Serialise them on one stream. Each call zeroes the counters it needs.
+ *   - Device error bits (an ignored out-of-range write_slot) stay in the
+ *     static array and are not reported by lf_device_errors.
+ */
+lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, int32_t* mask,
+                                 const void* new_k, const void* new_v,
+                                 const int32_t* write_slot, void* out, int32_t* next_slot,
+                                 int B, int Hq, int Hkv, int d, int S, int W, float scale,
+                                 void* stream);
+
+/*
  * Read (and optionally clear) the device error word of `stream`'s scratch.
  * Synchronises the stream. *flags receives an OR of LF_DEVERR_* bits, 0 if the
  * stream has never run a step.

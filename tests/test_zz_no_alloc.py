@@ -1,0 +1,88 @@
+"""The allocation-free entry point, lf_decode_step_noalloc, against lf_decode_step.
+
+Some callers cannot call cudaMalloc once they are running: a serving engine
+that hands all free GPU memory to its own pools at start-up has none left,
+and a real-time decode loop may not accept the device-wide synchronisation
+that cudaMalloc and cudaFree can cause. lf_decode_step_noalloc serves them by
+keeping its scratch in a fixed array compiled into the library. These tests
+call it through the C ABI and check that two calls in a row give the same
+result as the allocating entry point, within the tolerances the other GPU
+tests use, and that a shape whose scratch does not fit is refused.
+
+This file is collected last on purpose: if it fails, a run that stops at the
+first failure has already run every other test.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import decode_kv_cache_step_gb300 as lf
+from decode_kv_cache_step_gb300.workloads import WORKLOADS, initial_state, step_inputs
+
+from _gpu import OUT_ATOL, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _state(st):
+    return {"k": to_dev(st["k_cache"]), "v": to_dev(st["v_cache"]), "mask": to_dev(st["mask"])}
+
+
+def test_noalloc_matches_lf_decode_step_on_two_calls_in_a_row():
+    wl = WORKLOADS["qwen3_8b_b128_s3200"].with_batch(8)
+    st = initial_state(wl)
+    lib = lf.load_library()
+    ref, got = _state(st), _state(st)
+    shape = (wl.B, wl.Hq, wl.d)
+    out_ref = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    out_got = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    ws_ref = torch.full((wl.B, wl.Hkv), -1, dtype=torch.int32, device="cuda")
+    ws_got = ws_ref.clone()
+    nxt_ref = torch.empty_like(ws_ref)
+    nxt_got = torch.empty_like(ws_ref)
+    stream = torch.cuda.current_stream().cuda_stream
+    for call in range(2):
+        inp = step_inputs(wl, call)
+        q, nk, nv = to_dev(inp["q"]), to_dev(inp["new_k"]), to_dev(inp["new_v"])
+        lf.decode_step(q, ref["k"], ref["v"], ref["mask"], nk, nv, ws_ref, out_ref, nxt_ref,
+                       wl.W, wl.scale)
+        rc = lib.lf_decode_step_noalloc(
+            q.data_ptr(), got["k"].data_ptr(), got["v"].data_ptr(), got["mask"].data_ptr(),
+            nk.data_ptr(), nv.data_ptr(), ws_got.data_ptr(), out_got.data_ptr(),
+            nxt_got.data_ptr(), wl.B, wl.Hq, wl.Hkv, wl.d, wl.S, wl.W, ctypes.c_float(wl.scale),
+            stream)
+        assert rc == lf.LF_OK, lib.lf_last_error().decode()
+        torch.cuda.synchronize()
+        err = (out_got.float() - out_ref.float()).abs().max().item()
+        assert err <= OUT_ATOL, f"call {call}: output differs by {err}"
+        assert torch.equal(nxt_got, nxt_ref), f"call {call}: next_slot differs"
+        assert torch.equal(got["mask"], ref["mask"]), f"call {call}: mask differs"
+        assert torch.equal(got["k"], ref["k"]) and torch.equal(got["v"], ref["v"])
+        if call == 1:
+            assert (ws_got >= 0).all()  # the second call really wrote new tokens
+        ws_ref.copy_(nxt_ref)
+        ws_got.copy_(nxt_got)
+
+
+def test_noalloc_refuses_a_shape_whose_scratch_does_not_fit():
+    # One sequence, 8 KV heads x 4 query heads, 2^17 slots: the per-slot score
+    # terms alone need 16 MiB. The buffers are real, so nothing could fault
+    # even if the size check were missing.
+    B, Hq, Hkv, d, S = 1, 32, 8, 128, 1 << 17
+    lib = lf.load_library()
+    q = torch.zeros(B, Hq, d, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(B, Hkv, S, d, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
+    mask = torch.zeros(B, Hkv, S, dtype=torch.int32, device="cuda")
+    nk = torch.zeros(B, Hkv, d, dtype=torch.bfloat16, device="cuda")
+    nv = torch.zeros_like(nk)
+    ws = torch.full((B, Hkv), -1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    nxt = torch.empty_like(ws)
+    rc = lib.lf_decode_step_noalloc(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), mask.data_ptr(), nk.data_ptr(), nv.data_ptr(),
+        ws.data_ptr(), out.data_ptr(), nxt.data_ptr(), B, Hq, Hkv, d, S, 0,
+        ctypes.c_float(0.088), torch.cuda.current_stream().cuda_stream)
+    assert rc == lf.LF_ERR_UNSUPPORTED
+    assert "static scratch" in lib.lf_last_error().decode()

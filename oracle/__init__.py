@@ -62,6 +62,8 @@ def _bind(path):
     i = ctypes.c_int
     lib.lfo_decode_step.argtypes = [P] * 11 + [i] * 6 + [ctypes.c_float, i, P, i]
     lib.lfo_decode_step.restype = i
+    lib.lfo_decode_step_ex.argtypes = [P] * 11 + [i] * 6 + [ctypes.c_float] + [i] * 5 + [P, i]
+    lib.lfo_decode_step_ex.restype = i
     lib.lfo_max_threads.argtypes = []
     lib.lfo_max_threads.restype = i
     return lib
@@ -96,7 +98,8 @@ def _need(a, dtype, shape, name):
 
 
 def decode_step(q, k_cache, v_cache, mask, new_k, new_v, write_slot, W, scale, *,
-                want_p=False, want_scores=False, nthreads=0, units=None, lib=None):
+                want_p=False, want_scores=False, nthreads=0, units=None, lib=None,
+                topk=1, fill_first=False, mask_evicted=False, attention_only=False):
     """Run one decode step in fp64.
 
     bf16 arrays are numpy ``uint16`` bit patterns. ``k_cache``, ``v_cache`` and
@@ -108,6 +111,13 @@ def decode_step(q, k_cache, v_cache, mask, new_k, new_v, write_slot, W, scale, *
     ``invalid_writes`` int, and ``p`` [B,Hq,S] / ``scores`` [B,Hkv,S] on request
     (scores are +inf on masked slots). ``lib`` selects another build bound with
     ``bind_library``.
+
+    Options: ``topk`` > 1 returns ``next_slot`` as [B,Hkv,topk], the topk
+    candidates in ascending (class, score, slot) order, -1 past the last;
+    ``fill_first`` makes empty slots candidates ranked before every score;
+    ``mask_evicted`` sets the mask of returned slots to -1; ``attention_only``
+    writes and attends only (the written slot becomes live, nothing ages, no
+    selection; ``next_slot`` is None).
     """
     B, Hq, d = q.shape
     _, Hkv, S, _ = k_cache.shape
@@ -119,20 +129,25 @@ def decode_step(q, k_cache, v_cache, mask, new_k, new_v, write_slot, W, scale, *
     _need(new_v, np.uint16, (B, Hkv, d), "new_v")
     _need(write_slot, np.int32, (B, Hkv), "write_slot")
     out = np.full((B, Hq, d), np.nan, dtype=np.float64)
-    nxt = np.full((B, Hkv), -2, dtype=np.int32)
+    nxt = np.full((B, Hkv, int(topk)), -2, dtype=np.int32)
     p = np.zeros((B, Hq, S), dtype=np.float64) if want_p else None
     sc = np.full((B, Hkv, S), np.nan, dtype=np.float64) if want_scores else None
     u = None
     if units is not None:
         u = np.ascontiguousarray(np.asarray(units, dtype=np.int32))
-    rc = (lib or _load()).lfo_decode_step(
+    rc = (lib or _load()).lfo_decode_step_ex(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(mask), _ptr(new_k), _ptr(new_v),
         _ptr(write_slot), _ptr(out), _ptr(nxt), _ptr(p), _ptr(sc), B, Hq, Hkv, d, S, int(W),
-        float(scale), int(nthreads), _ptr(u), 0 if u is None else int(u.size))
+        float(scale), int(topk), int(bool(fill_first)), int(bool(mask_evicted)),
+        int(bool(attention_only)), int(nthreads), _ptr(u), 0 if u is None else int(u.size))
     if rc == -1:
         raise ValueError("oracle: invalid arguments")
     if rc == -2:
         raise MemoryError("oracle: out of memory")
+    if attention_only:
+        nxt = None
+    elif topk == 1:
+        nxt = np.ascontiguousarray(nxt[:, :, 0])
     res = {"out": out, "next_slot": nxt, "invalid_writes": int(rc)}
     if want_p:
         res["p"] = p

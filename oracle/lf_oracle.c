@@ -52,6 +52,30 @@
 #include <omp.h>
 #endif
 
+/* What a step returns besides the output (see lfo_decode_step_ex). */
+typedef struct {
+    int topk;           /* slots returned per unit */
+    int fill_first;     /* empty slots are returned first, lowest index first */
+    int mask_evicted;   /* returned slots get mask -1 */
+    int attention_only; /* no score, no selection, no ageing */
+} oracle_opts;
+
+/* A selection candidate: class 0 = empty slot (fill), class 1 = scored slot. */
+typedef struct {
+    int cls;
+    double score;
+    int slot;
+} candidate;
+
+/* Ascending (class, score, slot): the plain order the selection follows. */
+static int cmp_candidate(const void* pa, const void* pb) {
+    const candidate* a = (const candidate*)pa;
+    const candidate* b = (const candidate*)pb;
+    if (a->cls != b->cls) return a->cls < b->cls ? -1 : 1;
+    if (a->score != b->score) return a->score < b->score ? -1 : 1;
+    return (a->slot > b->slot) - (a->slot < b->slot);
+}
+
 /* Widen a bf16 bit pattern to double (exact). */
 static double bf16_to_double(uint16_t bits) {
     uint32_t u = (uint32_t)bits << 16;
@@ -66,7 +90,7 @@ static int oracle_unit(int b, int kvh, const uint16_t* q, uint16_t* k_cache, uin
                        int32_t* mask, const uint16_t* new_k, const uint16_t* new_v,
                        const int32_t* write_slot, double* out, int32_t* next_slot,
                        double* p_out, double* score_out, int Hq, int Hkv, int d, int S, int W,
-                       double scale) {
+                       double scale, const oracle_opts* opt) {
     const int g = Hq / Hkv;
     const size_t unit = (size_t)b * Hkv + kvh;
     uint16_t* K = k_cache + unit * (size_t)S * d;
@@ -83,11 +107,16 @@ static int oracle_unit(int b, int kvh, const uint16_t* q, uint16_t* k_cache, uin
     if (ws >= 0) {
         memcpy(K + (size_t)ws * d, new_k + unit * (size_t)d, sizeof(uint16_t) * (size_t)d);
         memcpy(V + (size_t)ws * d, new_v + unit * (size_t)d, sizeof(uint16_t) * (size_t)d);
-        for (int j = 0; j < S; ++j) {
-            if (j == ws)
-                age[j] = 0;
-            else if (age[j] >= 0 && age[j] < INT32_MAX)
-                age[j] += 1;
+        if (opt->attention_only) {
+            /* Attention alone: the written slot is live; nothing else ages. */
+            if (age[ws] < 0) age[ws] = 0;
+        } else {
+            for (int j = 0; j < S; ++j) {
+                if (j == ws)
+                    age[j] = 0;
+                else if (age[j] >= 0 && age[j] < INT32_MAX)
+                    age[j] += 1;
+            }
         }
     }
 
@@ -154,54 +183,76 @@ static int oracle_unit(int b, int kvh, const uint16_t* q, uint16_t* k_cache, uin
             for (int j = 0; j < S; ++j) p_out[((size_t)b * Hq + hq) * S + j] = p[j];
     }
 
-    /* Step 6: evict. argmin of I over live slots with age >= W; the lowest
-     * index wins a tie because only a strictly smaller score replaces the best. */
-    int best = -1;
-    double best_score = INFINITY;
-    for (int j = 0; j < S; ++j) {
-        if (age[j] < 0 || age[j] < W) continue;
-        if (best < 0 || I[j] < best_score) {
-            best = j;
-            best_score = I[j];
-        }
-    }
-    next_slot[unit] = best;
-
     if (score_out)
         for (int j = 0; j < S; ++j)
             score_out[unit * (size_t)S + j] = (age[j] >= 0) ? I[j] : INFINITY;
+
+    /* Step 6: evict. The candidates are the live slots with age >= W (and,
+     * when filling first, the empty slots, ranked before every score). They
+     * are sorted by (class, I, slot) and the first topk are returned: topk = 1
+     * is the argmin of I with ties to the lowest slot. */
+    if (!opt->attention_only) {
+        candidate* cand = (candidate*)malloc(sizeof(candidate) * (size_t)S);
+        if (!cand) {
+            free(s); free(p); free(G); free(I);
+            return -1;
+        }
+        int nc = 0;
+        for (int j = 0; j < S; ++j) {
+            if (age[j] >= 0 && age[j] >= W) {
+                cand[nc].cls = 1; cand[nc].score = I[j]; cand[nc].slot = j; ++nc;
+            } else if (age[j] < 0 && opt->fill_first) {
+                cand[nc].cls = 0; cand[nc].score = 0.0; cand[nc].slot = j; ++nc;
+            }
+        }
+        qsort(cand, (size_t)nc, sizeof(candidate), cmp_candidate);
+        for (int i = 0; i < opt->topk; ++i) {
+            const int slot = (i < nc) ? cand[i].slot : -1;
+            next_slot[unit * (size_t)opt->topk + i] = slot;
+            if (slot >= 0 && opt->mask_evicted) age[slot] = -1;
+        }
+        free(cand);
+    }
 
     free(s); free(p); free(G); free(I);
     return invalid;
 }
 
 /*
- * One decode step over the whole batch.
+ * One decode step over the whole batch, with a choice of what it returns.
  *
  * q [B][Hq][d], new_k/new_v [B][Hkv][d]: bf16 bits. k_cache/v_cache
  * [B][Hkv][S][d] bf16 bits and mask [B][Hkv][S] are updated in place.
- * write_slot/next_slot [B][Hkv]. out [B][Hq][d] double.
+ * write_slot [B][Hkv]. out [B][Hq][d] double.
+ * next_slots [B][Hkv][topk]: the topk candidates in ascending (class, score,
+ * slot) order, -1 past the last; untouched when attention_only.
  * p_out [B][Hq][S] (optional): final softmax weights, 0 on masked slots.
  * score_out [B][Hkv][S] (optional): I_j on live slots, +inf on masked slots.
+ * fill_first: empty slots are candidates ranked before every score (the
+ * cache-fill phase). mask_evicted: returned slots get mask -1. topk > 1: the
+ * periodic k-at-once compression. attention_only: write and attend only.
  * units/n_units (optional): process only these unit indices (b * Hkv + kvh);
  * outputs of other units are left untouched.
  *
  * Returns the number of invalid write slots seen (>= 0), -1 for bad arguments,
  * -2 if memory ran out.
  */
-int lfo_decode_step(const uint16_t* q, uint16_t* k_cache, uint16_t* v_cache, int32_t* mask,
-                    const uint16_t* new_k, const uint16_t* new_v, const int32_t* write_slot,
-                    double* out, int32_t* next_slot, double* p_out, double* score_out, int B,
-                    int Hq, int Hkv, int d, int S, int W, float scale, int nthreads,
-                    const int32_t* units, int n_units) {
-    if (!q || !k_cache || !v_cache || !mask || !new_k || !new_v || !write_slot || !out ||
-        !next_slot)
+int lfo_decode_step_ex(const uint16_t* q, uint16_t* k_cache, uint16_t* v_cache, int32_t* mask,
+                       const uint16_t* new_k, const uint16_t* new_v, const int32_t* write_slot,
+                       double* out, int32_t* next_slots, double* p_out, double* score_out,
+                       int B, int Hq, int Hkv, int d, int S, int W, float scale, int topk,
+                       int fill_first, int mask_evicted, int attention_only, int nthreads,
+                       const int32_t* units, int n_units) {
+    if (!q || !k_cache || !v_cache || !mask || !new_k || !new_v || !write_slot || !out)
         return -1;
-    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || d < 1 || S < 1 || W < 0) return -1;
+    if (!attention_only && !next_slots) return -1;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || d < 1 || S < 1 || W < 0 || topk < 1)
+        return -1;
     const int total = (units != NULL) ? n_units : B * Hkv;
     if (units != NULL)
         for (int i = 0; i < n_units; ++i)
             if (units[i] < 0 || units[i] >= B * Hkv) return -1;
+    const oracle_opts opt = {topk, fill_first != 0, mask_evicted != 0, attention_only != 0};
     const double dscale = (double)scale;
     int invalid = 0, oom = 0;
 #ifdef _OPENMP
@@ -211,8 +262,8 @@ int lfo_decode_step(const uint16_t* q, uint16_t* k_cache, uint16_t* v_cache, int
     for (int i = 0; i < total; ++i) {
         const int u = (units != NULL) ? units[i] : i;
         const int r = oracle_unit(u / Hkv, u % Hkv, q, k_cache, v_cache, mask, new_k, new_v,
-                                  write_slot, out, next_slot, p_out, score_out, Hq, Hkv, d, S,
-                                  W, dscale);
+                                  write_slot, out, next_slots, p_out, score_out, Hq, Hkv, d, S,
+                                  W, dscale, &opt);
         if (r < 0)
             oom += 1;
         else
@@ -220,6 +271,18 @@ int lfo_decode_step(const uint16_t* q, uint16_t* k_cache, uint16_t* v_cache, int
     }
     (void)nthreads;
     return oom ? -2 : invalid;
+}
+
+/* The LongFlow step as in the paper: one evicted slot per unit (the argmin). */
+int lfo_decode_step(const uint16_t* q, uint16_t* k_cache, uint16_t* v_cache, int32_t* mask,
+                    const uint16_t* new_k, const uint16_t* new_v, const int32_t* write_slot,
+                    double* out, int32_t* next_slot, double* p_out, double* score_out, int B,
+                    int Hq, int Hkv, int d, int S, int W, float scale, int nthreads,
+                    const int32_t* units, int n_units) {
+    if (!next_slot) return -1;
+    return lfo_decode_step_ex(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slot,
+                              p_out, score_out, B, Hq, Hkv, d, S, W, scale, 1, 0, 0, 0, nthreads,
+                              units, n_units);
 }
 
 /* Threads the oracle would use for nthreads <= 0. */

@@ -83,11 +83,11 @@ def f(bits):
 # brute force (pure Python, tiny sizes only)
 # ---------------------------------------------------------------------------
 
-def brute_force(case, W, scale):
+def brute_force(case, W, scale, topk=1, fill_first=False, mask_evicted=False):
     """Pure-Python restatement, structured differently from the oracle.
 
-    Softmax without max-shift, score through (sum_h p) * ||v||_1, argmin by
-    sorting (score, index) pairs, state kept in dicts.
+    Softmax without max-shift, score through (sum_h p) * ||v||_1, selection by
+    sorting (class, score, index) triples, state kept in dicts.
     """
     q, K, V = f(case["q"]), f(case["k_cache"]), f(case["v_cache"])
     nk, nv = f(case["new_k"]), f(case["new_v"])
@@ -95,7 +95,7 @@ def brute_force(case, W, scale):
     Hkv, S = K.shape[1], K.shape[2]
     g = Hq // Hkv
     out = np.zeros((B, Hq, d))
-    nxt = np.zeros((B, Hkv), dtype=np.int32)
+    nxt = np.zeros((B, Hkv, topk), dtype=np.int32)
     scores = np.full((B, Hkv, S), np.inf)
     ages_after = np.array(case["mask"], copy=True)
     for b in range(B):
@@ -120,10 +120,18 @@ def brute_force(case, W, scale):
                     psum[j] += e[j] / tot
             for j in live:
                 scores[b, kv, j] = psum[j] * sum(abs(x) for x in rows_v[j])
-            elig = sorted((scores[b, kv, j], j) for j in live if ages[j] >= W)
-            nxt[b, kv] = elig[0][1] if elig else -1
+            elig = [(1, scores[b, kv, j], j) for j in live if ages[j] >= W]
+            if fill_first:
+                elig += [(0, 0.0, j) for j in range(S) if ages[j] < 0]
+            elig.sort()
+            for i in range(topk):
+                nxt[b, kv, i] = elig[i][2] if i < len(elig) else -1
+                if mask_evicted and i < len(elig):
+                    ages[elig[i][2]] = -1
             for j in range(S):
                 ages_after[b, kv, j] = ages[j]
+    if topk == 1:
+        nxt = nxt[:, :, 0]
     return {"out": out, "next_slot": nxt, "scores": scores, "mask": ages_after}
 
 
@@ -407,6 +415,89 @@ def check_multi_step_invariants(step):
         ws = res["next_slot"].copy()
 
 
+def check_brute_force_selection_options(step):
+    """Top-k, fill-empty-first and mask-evicted against the brute force."""
+    shapes = [(1, 2, 1, 3, 9), (2, 4, 2, 2, 7), (1, 6, 2, 2, 8), (2, 2, 1, 4, 12)]
+    opts = [dict(topk=3), dict(topk=2, fill_first=True), dict(topk=1, fill_first=True),
+            dict(topk=4, mask_evicted=True), dict(topk=20, fill_first=True, mask_evicted=True)]
+    for i, (shp, opt) in enumerate(zip(shapes * 2, opts)):
+        rng = np.random.default_rng(300 + i)
+        case = rand_case(rng, *shp, p_masked=0.3, max_age=12)
+        W = int(rng.integers(0, 3))
+        scale = float(np.float32(0.6))
+        res = run(step, case, W, scale, **opt)
+        ref = brute_force(case, W, scale, **opt)
+        assert np.array_equal(res["next_slot"], ref["next_slot"]), (opt, res["next_slot"], ref["next_slot"])
+        assert np.array_equal(res["state"]["mask"], ref["mask"]), opt
+        np.testing.assert_allclose(res["out"], ref["out"], rtol=0, atol=1e-12)
+
+
+def check_topk_properties(step):
+    rng = np.random.default_rng(31)
+    case = rand_case(rng, 2, 8, 2, 16, 60, p_masked=0.25, max_age=200)
+    base = run(step, case, 5, 0.3, want_scores=True)
+    for k in (1, 7, 64):
+        res = run(step, case, 5, 0.3, topk=k)
+        lst = res["next_slot"] if k > 1 else res["next_slot"][:, :, None]
+        ages = base["state"]["mask"]
+        for b in range(2):
+            for h in range(2):
+                elig = [j for j in range(60) if ages[b, h, j] >= 5]
+                want = sorted(elig, key=lambda j: (base["scores"][b, h, j], j))[:k]
+                got = [int(x) for x in lst[b, h] if x >= 0]
+                assert got == want, (k, got, want)
+                assert all(x == -1 for x in lst[b, h, len(want):])
+        if k == 1:
+            assert np.array_equal(res["next_slot"], base["next_slot"])
+
+
+def check_fill_first(step):
+    rng = np.random.default_rng(37)
+    case = rand_case(rng, 2, 4, 2, 8, 40, p_masked=0.0, max_age=100, ws_mode="none")
+    case["mask"][0, 0, [7, 3, 30]] = -1
+    res = run(step, case, 2, 0.3, fill_first=True)
+    plain = run(step, case, 2, 0.3)
+    assert res["next_slot"][0, 0] == 3                       # lowest empty slot first
+    assert np.array_equal(res["next_slot"][1], plain["next_slot"][1])   # no empty slot
+    assert res["next_slot"][0, 1] == plain["next_slot"][0, 1]
+    res3 = run(step, case, 2, 0.3, fill_first=True, topk=4)
+    assert list(res3["next_slot"][0, 0, :3]) == [3, 7, 30]
+    assert res3["next_slot"][0, 0, 3] == plain["next_slot"][0, 0]
+
+
+def check_mask_evicted(step):
+    rng = np.random.default_rng(41)
+    case = rand_case(rng, 1, 4, 2, 8, 30, p_masked=0.1, max_age=60)
+    plain = run(step, case, 3, 0.3, topk=5)
+    ev = run(step, case, 3, 0.3, topk=5, mask_evicted=True)
+    assert np.array_equal(plain["next_slot"], ev["next_slot"])
+    m_plain, m_ev = plain["state"]["mask"], ev["state"]["mask"]
+    for h in range(2):
+        chosen = [int(x) for x in ev["next_slot"][0, h] if x >= 0]
+        assert np.all(m_ev[0, h, chosen] == -1)
+        rest = [j for j in range(30) if j not in chosen]
+        assert np.array_equal(m_ev[0, h, rest], m_plain[0, h, rest])
+
+
+def check_attention_only(step):
+    rng = np.random.default_rng(43)
+    case = rand_case(rng, 2, 8, 2, 16, 50, p_masked=0.3, max_age=100, ws_mode="any")
+    full = run(step, case, 4, 0.25)
+    att = run(step, case, 4, 0.25, attention_only=True)
+    assert att["next_slot"] is None
+    np.testing.assert_array_equal(att["out"], full["out"])
+    m0, m1 = case["mask"], att["state"]["mask"]
+    for b in range(2):
+        for h in range(2):
+            ws = case["write_slot"][b, h]
+            for j in range(50):
+                if j == ws and m0[b, h, j] < 0:
+                    assert m1[b, h, j] == 0
+                else:
+                    assert m1[b, h, j] == m0[b, h, j]
+            assert np.array_equal(att["state"]["k_cache"][b, h], full["state"]["k_cache"][b, h])
+
+
 def _frac(s):
     return Fraction(s)
 
@@ -459,7 +550,8 @@ ALL_CHECKS = [
     check_masked_garbage_is_inert, check_zero_v_scores_zero_and_ties_lowest,
     check_protected_window, check_uniform_closed_form, check_score_sum_when_l1_constant,
     check_permutation_equivariance, check_state_transition, check_degenerate,
-    check_multi_step_invariants,
+    check_multi_step_invariants, check_brute_force_selection_options, check_topk_properties,
+    check_fill_first, check_mask_evicted, check_attention_only,
 ] + [
     (lambda name: (lambda step: check_golden(step, name)))(n) for n in GOLDEN_FILES
 ]

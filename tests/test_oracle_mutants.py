@@ -18,8 +18,17 @@ MUTANTS = [
     ("wrong_sign_in_exp", "exp(s[j] - smax)", "exp(smax - s[j])"),
     ("strided_gqa_grouping", "const int hq = kvh * g + h;", "const int hq = h * Hkv + kvh;"),
     ("score_without_abs", "acc += fabs(G[", "acc += (G["),
-    ("protected_window_off_by_one", "age[j] < W) continue;", "age[j] <= W) continue;"),
-    ("ties_to_highest_index", "I[j] < best_score", "I[j] <= best_score"),
+    ("protected_window_off_by_one", "age[j] >= 0 && age[j] >= W) {", "age[j] >= 0 && age[j] > W) {"),
+    ("ties_to_highest_index", "return (a->slot > b->slot) - (a->slot < b->slot);",
+     "return (a->slot < b->slot) - (a->slot > b->slot);"),
+    ("highest_scores_selected", "return a->score < b->score ? -1 : 1;", "return a->score < b->score ? 1 : -1;"),
+    ("empty_slots_ranked_last", "cand[nc].cls = 0;", "cand[nc].cls = 2;"),
+    ("evicted_slots_not_masked", "if (slot >= 0 && opt->mask_evicted) age[slot] = -1;", "if (0) age[slot] = -1;"),
+    ("topk_list_shifted", "const int slot = (i < nc) ? cand[i].slot : -1;",
+     "const int slot = (i + 1 < nc) ? cand[i + 1].slot : -1;"),
+    ("attention_only_resets_live_age", "if (age[ws] < 0) age[ws] = 0;", "age[ws] = 0;"),
+    ("attention_only_still_ages", "if (opt->attention_only) {\n            /* Attention alone",
+     "if (0) {\n            /* Attention alone"),
     ("no_ageing", "age[j] += 1;", "age[j] += 0;"),
     ("new_k_not_written", "memcpy(K + (size_t)ws * d, new_k", "if (0) memcpy(K + (size_t)ws * d, new_k"),
     ("new_v_not_written", "memcpy(V + (size_t)ws * d, new_v", "if (0) memcpy(V + (size_t)ws * d, new_v"),

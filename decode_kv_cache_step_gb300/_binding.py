@@ -26,12 +26,18 @@ LF_DEVERR_BAD_WRITE_SLOT = 0x1
 LF_DEVERR_WAIT_TIMEOUT = 0x2
 
 LF_KERNEL_DECODE_STEP = 0
-KERNEL_NAMES = {LF_KERNEL_DECODE_STEP: "lf_decode_step_kernel"}
+LF_KERNEL_ATTENTION = 1
+KERNEL_NAMES = {LF_KERNEL_DECODE_STEP: "lf_decode_step_kernel",
+                LF_KERNEL_ATTENTION: "lf_decode_step_kernel (attention-only variant)"}
+
+LF_STEP_FILL_EMPTY_FIRST = 0x1
+LF_STEP_MASK_EVICTED = 0x2
+LF_MAX_TOPK = 1024
 
 # Every exported symbol of include/lf_decode.h.
 EXPORTED = (
-    "lf_decode_step", "lf_decode_step_scores", "lf_decode_step_host", "lf_decode_step_noalloc",
-    "lf_device_errors",
+    "lf_decode_step", "lf_decode_step_scores", "lf_decode_step_ex", "lf_decode_attention",
+    "lf_decode_step_host", "lf_decode_step_noalloc", "lf_device_errors",
     "lf_profile_enable", "lf_profile_collect", "lf_release_workspace", "lf_status_string",
     "lf_last_error", "lf_version",
 )
@@ -72,6 +78,10 @@ def load_library(path: str | None = None):
         lib.lf_decode_step_noalloc.argtypes = step_args
         lib.lf_decode_step_noalloc.restype = I
         lib.lf_decode_step_scores.argtypes = [P] * 10 + [I] * 6 + [F, P]
+        lib.lf_decode_step_ex.argtypes = [P] * 9 + [I, I, P] + [I] * 6 + [F, P]
+        lib.lf_decode_step_ex.restype = I
+        lib.lf_decode_attention.argtypes = [P] * 8 + [I] * 5 + [F, P]
+        lib.lf_decode_attention.restype = I
         for fn in (lib.lf_decode_step, lib.lf_decode_step_host, lib.lf_decode_step_scores):
             fn.restype = I
         lib.lf_device_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I]
@@ -133,7 +143,7 @@ def _shapes(q, k_cache):
 
 
 def _check_step(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slot,
-                io_on_device=True):
+                io_on_device=True, k=None):
     B, Hq, Hkv, d, S = _shapes(q, k_cache)
     bf, i32 = torch.bfloat16, torch.int32
     _need(q, "q", bf, (B, Hq, d), io_on_device)
@@ -144,7 +154,7 @@ def _check_step(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_s
     _need(new_v, "new_v", bf, (B, Hkv, d), io_on_device)
     _need(write_slot, "write_slot", i32, (B, Hkv), io_on_device)
     _need(out, "out", bf, (B, Hq, d), io_on_device)
-    _need(next_slot, "next_slot", i32, (B, Hkv), io_on_device)
+    _need(next_slot, "next_slot", i32, (B, Hkv) if k is None else (B, Hkv, int(k)), io_on_device)
     return B, Hq, Hkv, d, S
 
 
@@ -171,6 +181,42 @@ def decode_step_scores(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out,
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), mask.data_ptr(), new_k.data_ptr(),
         new_v.data_ptr(), write_slot.data_ptr(), out.data_ptr(), next_slot.data_ptr(),
         scores.data_ptr(), B, Hq, Hkv, d, S, int(W), float(scale), _stream_handle(stream)))
+
+
+def decode_step_ex(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slots, W,
+                   scale, k=1, flags=0, scores=None, stream=None):
+    """lf_decode_step_ex: next_slots [B,Hkv,k] int32 gets the k lowest-(score, slot)
+    candidates per unit; flags are LF_STEP_* bits; scores optional [B,Hkv,S]."""
+    lib = load_library()
+    B, Hq, Hkv, d, S = _check_step(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out,
+                                   next_slots, k=k)
+    if scores is not None:
+        _need(scores, "scores", torch.float32, (B, Hkv, S), True)
+    _check(lib, lib.lf_decode_step_ex(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), mask.data_ptr(), new_k.data_ptr(),
+        new_v.data_ptr(), write_slot.data_ptr(), out.data_ptr(), next_slots.data_ptr(), int(k),
+        int(flags), None if scores is None else scores.data_ptr(), B, Hq, Hkv, d, S, int(W),
+        float(scale), _stream_handle(stream)))
+
+
+def decode_attention(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, scale,
+                     stream=None):
+    """lf_decode_attention: slot write and attention only (no score, no eviction)."""
+    lib = load_library()
+    B, Hq, Hkv, d, S = _shapes(q, k_cache)
+    bf, i32 = torch.bfloat16, torch.int32
+    _need(q, "q", bf, (B, Hq, d), True)
+    _need(k_cache, "k_cache", bf, (B, Hkv, S, d), True)
+    _need(v_cache, "v_cache", bf, (B, Hkv, S, d), True)
+    _need(mask, "mask", i32, (B, Hkv, S), True)
+    _need(new_k, "new_k", bf, (B, Hkv, d), True)
+    _need(new_v, "new_v", bf, (B, Hkv, d), True)
+    _need(write_slot, "write_slot", i32, (B, Hkv), True)
+    _need(out, "out", bf, (B, Hq, d), True)
+    _check(lib, lib.lf_decode_attention(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), mask.data_ptr(), new_k.data_ptr(),
+        new_v.data_ptr(), write_slot.data_ptr(), out.data_ptr(), B, Hq, Hkv, d, S, float(scale),
+        _stream_handle(stream)))
 
 
 def decode_step_host(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slot, W,

@@ -262,6 +262,9 @@ struct StepArgs {
     void* out;
     int32_t* next_slot;
     float* scores;
+    int topk = 1;        // slots returned per unit into next_slot[B][Hkv][topk]
+    int flags = 0;       // LF_STEP_* bits
+    bool score = true;   // false: attention only (no score, no eviction, no ageing)
 };
 
 lf_status check_args(const StepArgs& a, const Shape& s) {
@@ -274,8 +277,12 @@ lf_status check_args(const StepArgs& a, const Shape& s) {
     if ((st = check_ptr(a.new_v, 16, "new_v")) != LF_OK) return st;
     if ((st = check_ptr(a.write_slot, 4, "write_slot")) != LF_OK) return st;
     if ((st = check_ptr(a.out, 16, "out")) != LF_OK) return st;
-    if ((st = check_ptr(a.next_slot, 4, "next_slot")) != LF_OK) return st;
+    if (a.score && (st = check_ptr(a.next_slot, 4, "next_slot")) != LF_OK) return st;
     if (a.scores && !aligned(a.scores, 4)) return fail(LF_ERR_INVALID_ARG, "scores is not 4-byte aligned");
+    if (a.topk < 1 || a.topk > LF_MAX_TOPK)
+        return fail(LF_ERR_INVALID_ARG, "k = %d is outside [1, %d]", a.topk, LF_MAX_TOPK);
+    if (a.flags & ~(LF_STEP_FILL_EMPTY_FIRST | LF_STEP_MASK_EVICTED))
+        return fail(LF_ERR_INVALID_ARG, "unknown flag bits 0x%x", a.flags);
     return check_shape(s);
 }
 
@@ -328,11 +335,17 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
     sp.nchunk = pl.nchunk;
     sp.chunk_tiles = pl.chunk_tiles;
     sp.scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
+    sp.topk = a.score ? a.topk : 1;
+    sp.flags = a.score ? a.flags : 0;
+    if (!lf::step_fits(s.d, g, pl.stages, a.score, pl.nchunk, sp.topk))
+        return fail(LF_ERR_UNSUPPORTED,
+                    "k = %d with %d chunks of the slot axis does not fit in shared memory",
+                    sp.topk, pl.nchunk);
 
     cudaError_t e;
     {
-        ProfScope prof(LF_KERNEL_DECODE_STEP, stream);
-        e = lf::launch_decode_step(s.d, g, pl.stages, tmK, tmV, sp, units, stream);
+        ProfScope prof(a.score ? LF_KERNEL_DECODE_STEP : LF_KERNEL_ATTENTION, stream);
+        e = lf::launch_decode_step(s.d, g, pl.stages, a.score, tmK, tmV, sp, units, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");
     return LF_OK;
@@ -401,6 +414,26 @@ lf_status lf_decode_step_scores(const void* q, void* k_cache, void* v_cache, int
     if (!scores) return fail(LF_ERR_INVALID_ARG, "scores is NULL");
     StepArgs a{q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slot, scores};
     return run_step(a, Shape{B, Hq, Hkv, d, S, W, scale}, stream);
+}
+
+lf_status lf_decode_step_ex(const void* q, void* k_cache, void* v_cache, int32_t* mask,
+                            const void* new_k, const void* new_v, const int32_t* write_slot,
+                            void* out, int32_t* next_slots, int k, int flags, float* scores,
+                            int B, int Hq, int Hkv, int d, int S, int W, float scale,
+                            void* stream) {
+    StepArgs a{q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slots, scores};
+    a.topk = k;
+    a.flags = flags;
+    return run_step(a, Shape{B, Hq, Hkv, d, S, W, scale}, stream);
+}
+
+lf_status lf_decode_attention(const void* q, void* k_cache, void* v_cache, int32_t* mask,
+                              const void* new_k, const void* new_v, const int32_t* write_slot,
+                              void* out, int B, int Hq, int Hkv, int d, int S, float scale,
+                              void* stream) {
+    StepArgs a{q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, nullptr, nullptr};
+    a.score = false;
+    return run_step(a, Shape{B, Hq, Hkv, d, S, 0, scale}, stream);
 }
 
 lf_status lf_decode_step_host(const void* q_host, void* k_cache, void* v_cache, int32_t* mask,
@@ -510,7 +543,9 @@ lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, in
     sp.chunk_tiles = pl.chunk_tiles;
     sp.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     g_last_error[0] = '\0';
-    e = lf::launch_decode_step(d, g, pl.stages, tmK, tmV, sp, static_cast<int>(units), stream);
+    sp.topk = 1;
+    sp.flags = 0;
+    e = lf::launch_decode_step(d, g, pl.stages, true, tmK, tmV, sp, static_cast<int>(units), stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");
     return LF_OK;
 }

@@ -30,9 +30,15 @@
 //   NaN or Inf in masked rows never reaches the output.
 // The CTA then publishes its chunk's (m, l, O) and counts itself in. The last
 // CTA of the unit merges the chunks, writes the output row, finishes
-// LongFlowScore for every live slot, reduces the lexicographic (I_j, j)
-// argmin over slots with age >= W and drops the unit's scratch lines from L2
-// without writing them back.
+// LongFlowScore for every live slot, selects the slots to evict and drops the
+// unit's scratch lines from L2 without writing them back. The selection is
+// the lexicographic (I_j, j) argmin over slots with age >= W, or, for k > 1,
+// the k smallest by an 8-bit radix select on the score bits (then on the slot
+// index among equal scores) and a bitonic sort of the k winners; the periodic
+// k-at-once compression of the Fig. 3 caption. Empty slots can rank first
+// (cache-fill phase) and the chosen slots can be masked in place.
+// An attention-only instantiation (kScore = false) drops the row norms, the
+// score terms, the ageing and the selection: the baseline for the overhead.
 #include <math.h>
 
 #include "../../include/lf_decode.h"
@@ -109,8 +115,142 @@ __device__ __forceinline__ void discard_range(const void* p, size_t bytes, int t
         discard_l2_line(reinterpret_cast<const void*>(line));
 }
 
+// Lexicographic (key, slot) order for the top-k list.
+__device__ __forceinline__ bool key_less(uint32_t ka, int ja, uint32_t kb, int jb) {
+    return ka < kb || (ka == kb && ja < jb);
+}
+
+// One 8-bit radix-select pass over the unit's candidate keys: among values v
+// with (v & pmask) == prefix, finds the digit (v >> shift) & 255 holding the
+// `remaining`-th smallest and returns the rank left inside that digit. With
+// by_slot the value is the slot index of keys equal to `tie_key`.
+__device__ __forceinline__ int radix_pass(const uint32_t* keys, int stride, int S, int shift,
+                                          uint32_t pmask, uint32_t prefix, int remaining,
+                                          bool by_slot, uint32_t tie_key, int* hist,
+                                          int* s_out, int tid, uint32_t* digit_out) {
+    for (int i = tid; i < 256; i += kConsumers) hist[i] = 0;
+    consumer_bar_sync();
+    for (int j = tid; j < S; j += kConsumers) {
+        const uint32_t key = __ldcg(keys + static_cast<size_t>(j) * stride);
+        if (key == 0xffffffffu) continue;
+        const uint32_t v = by_slot ? static_cast<uint32_t>(j) : key;
+        if (by_slot && key != tie_key) continue;
+        if ((v & pmask) == prefix) atomicAdd(&hist[(v >> shift) & 255], 1);
+    }
+    consumer_bar_sync();
+    if (tid == 0) {
+        int cum = 0, d = 255;
+        for (int b = 0; b < 256; ++b) {
+            if (cum + hist[b] >= remaining) {
+                d = b;
+                break;
+            }
+            cum += hist[b];
+        }
+        s_out[0] = d;
+        s_out[1] = remaining - cum;
+    }
+    consumer_bar_sync();
+    *digit_out = static_cast<uint32_t>(s_out[0]);
+    return s_out[1];
+}
+
+// The k smallest (key, slot) pairs of a unit, ascending, into next_slot[u][k]
+// (-1 past the number of candidates). Keys were written one per slot (stride
+// `stride` words); 0xffffffff marks a slot that is not a candidate.
+__device__ void select_topk(const StepParams& p, int u, const uint32_t* keys, int stride,
+                            int ncand, uint8_t* area, int tid) {
+    const int S = p.S;
+    const int k = p.topk;
+    int* hist = reinterpret_cast<int*>(area);              // [256]
+    int* s_out = hist + 256;                               // [4]
+    uint32_t* l_key = reinterpret_cast<uint32_t*>(s_out + 4);  // [kMaxTopK]
+    int* l_idx = reinterpret_cast<int*>(l_key + kMaxTopK);     // [kMaxTopK]
+    const int keff = min(k, ncand);
+    int32_t* out = p.next_slot + static_cast<size_t>(u) * k;
+    if (keff > 0) {
+        // Threshold key T: the keff-th smallest key.
+        uint32_t prefix = 0, pmask = 0;
+        int remaining = keff;
+        for (int pass = 0; pass < 4; ++pass) {
+            const int shift = 24 - 8 * pass;
+            uint32_t dgt;
+            remaining = radix_pass(keys, stride, S, shift, pmask, prefix, remaining, false, 0u,
+                                   hist, s_out, tid, &dgt);
+            prefix |= dgt << shift;
+            pmask |= 0xffu << shift;
+        }
+        const uint32_t T = prefix;
+        // Among keys equal to T, the `remaining` lowest slots: slot threshold J.
+        uint32_t iprefix = 0, ipmask = 0;
+        for (int pass = 0; pass < 3; ++pass) {
+            const int shift = 16 - 8 * pass;
+            uint32_t dgt;
+            remaining = radix_pass(keys, stride, S, shift, ipmask, iprefix, remaining, true, T,
+                                   hist, s_out, tid, &dgt);
+            iprefix |= dgt << shift;
+            ipmask |= 0xffu << shift;
+        }
+        const int J = static_cast<int>(iprefix);
+        if (tid == 0) s_out[2] = 0;
+        consumer_bar_sync();
+        for (int j = tid; j < S; j += kConsumers) {
+            const uint32_t key = __ldcg(keys + static_cast<size_t>(j) * stride);
+            if (key == 0xffffffffu) continue;
+            if (key < T || (key == T && j <= J)) {
+                const int pos = atomicAdd(&s_out[2], 1);
+                if (pos < kMaxTopK) {
+                    l_key[pos] = key;
+                    l_idx[pos] = j;
+                }
+            }
+        }
+        consumer_bar_sync();
+        // Bitonic sort of the keff winners by (key, slot).
+        int n2 = 1;
+        while (n2 < keff) n2 <<= 1;
+        for (int i = keff + tid; i < n2; i += kConsumers) {
+            l_key[i] = 0xffffffffu;
+            l_idx[i] = 0x7fffffff;
+        }
+        consumer_bar_sync();
+        for (int size = 2; size <= n2; size <<= 1) {
+            for (int stride2 = size >> 1; stride2 > 0; stride2 >>= 1) {
+                for (int i = tid; i < n2; i += kConsumers) {
+                    const int ixj = i ^ stride2;
+                    if (ixj > i) {
+                        const bool up = (i & size) == 0;
+                        const bool swap = up ? key_less(l_key[ixj], l_idx[ixj], l_key[i], l_idx[i])
+                                             : key_less(l_key[i], l_idx[i], l_key[ixj], l_idx[ixj]);
+                        if (swap) {
+                            const uint32_t tk = l_key[i];
+                            const int ti = l_idx[i];
+                            l_key[i] = l_key[ixj];
+                            l_idx[i] = l_idx[ixj];
+                            l_key[ixj] = tk;
+                            l_idx[ixj] = ti;
+                        }
+                    }
+                }
+                consumer_bar_sync();
+            }
+        }
+    }
+    for (int i = tid; i < k; i += kConsumers) {
+        const int slot = (i < keff) ? l_idx[i] : -1;
+        out[i] = slot;
+        if (slot >= 0 && (p.flags & kFlagMaskEvicted))
+            p.mask[static_cast<size_t>(u) * S + slot] = -1;
+    }
+}
+
+template <int G>
+__device__ void score_and_select(const StepParams& p, int u, const float* s_m, const float* s_il,
+                                 float* red_v, int* red_j, int* s_ncand, uint8_t* topk_area,
+                                 int tid);
+
 // Merge of the unit's chunks by its last CTA (consumer threads only).
-template <int D, int G>
+template <int D, int G, bool kScore>
 __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) {
     const int nchunk = p.nchunk;
     float* s_w = reinterpret_cast<float*>(smem);  // [nchunk][G]: 2^(m_c - m) / l
@@ -118,6 +258,9 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) 
     float* s_il = s_m + G;                        // [G]
     float* red_v = s_il + G;                      // [4]
     int* red_j = reinterpret_cast<int*>(red_v + kConsumerWarps);
+    int* s_ncand = red_j + kConsumerWarps;
+    uint8_t* topk_area = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(s_ncand + 4) + 15) & ~static_cast<uintptr_t>(15));
     const float2* ml = p.part_ml + static_cast<size_t>(u) * nchunk * G;
 
     if (tid < G) {
@@ -131,6 +274,7 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) 
         s_m[tid] = m;
         s_il[tid] = (l > 0.f) ? 1.f / l : 0.f;
     }
+    if (tid == 0) s_ncand[0] = 0;
     consumer_bar_sync();
     for (int e = tid; e < nchunk * G; e += kConsumers) {
         const float2 v = __ldcg(&ml[e]);
@@ -178,8 +322,21 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) 
         const int e = tid + k * kConsumers;
         if (e < G * D) out[e] = __float2bfloat16_rn(o[k]);
     }
+    if constexpr (kScore) score_and_select<G>(p, u, s_m, s_il, red_v, red_j, s_ncand, topk_area, tid);
+    consumer_bar_sync();
+    // Every read of the unit's scratch is done: drop the lines, no write-back.
+    discard_range(po, static_cast<size_t>(nchunk) * G * D * sizeof(float), tid, kConsumers);
+}
 
-    // LongFlowScore of every live slot; argmin over the eligible ones.
+// LongFlowScore of every live slot of unit u and the selection of the slots to
+// evict, by the unit's last CTA once the final (m_h, l_h) are known.
+template <int G>
+__device__ void score_and_select(const StepParams& p, int u, const float* s_m, const float* s_il,
+                                 float* red_v, int* red_j, int* s_ncand, uint8_t* topk_area,
+                                 int tid) {
+    // LongFlowScore of every live slot; selection over the candidates: live
+    // slots with age >= W and, with kFlagFillEmptyFirst, empty slots (ranked
+    // before every score, lowest slot first).
     float m[G], il[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -188,10 +345,15 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) 
     }
     const int S = p.S;
     const int32_t* age = p.mask + static_cast<size_t>(u) * S;
-    const float* stash = p.stash + static_cast<size_t>(u) * S * G;
+    float* stash = p.stash + static_cast<size_t>(u) * S * G;
+    // For top-k the slot's first stash word is reused for its selection key.
+    uint32_t* keys = reinterpret_cast<uint32_t*>(stash);
     float* scores = p.scores ? p.scores + static_cast<size_t>(u) * S : nullptr;
+    const bool fill_first = (p.flags & kFlagFillEmptyFirst) != 0;
+    const bool top1 = p.topk == 1;
     float best = INFINITY;
     int bestj = 0x7fffffff;
+    int ncand = 0;
     // Batches of kBatch slots per thread: all loads of a batch are in flight
     // together instead of one L2 round trip per slot.
     constexpr int kBatch = 8;
@@ -213,47 +375,75 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) 
             const int j = j0 + k * kConsumers;
             if (j >= S) break;
             float I = INFINITY;
+            bool cand = false;
+            float cval = 0.f;
             if (a[k] >= 0) {
                 I = 0.f;
 #pragma unroll
                 for (int h = 0; h < G; ++h) I += exp2f(t[k][h] - m[h]) * il[h];
-                if (a[k] >= p.W && better(I, j, best, bestj)) {
-                    best = I;
+                cand = a[k] >= p.W && !isnan(I);
+                cval = I;
+            } else if (fill_first) {
+                cand = true;
+                cval = -1.f;
+            }
+            if (top1) {
+                if (cand && better(cval, j, best, bestj)) {
+                    best = cval;
                     bestj = j;
                 }
+            } else {
+                keys[static_cast<size_t>(j) * G] =
+                    !cand ? 0xffffffffu : (cval < 0.f ? 0u : __float_as_uint(cval) + 1u);
+                ncand += cand ? 1 : 0;
             }
             if (scores) scores[j] = I;
         }
     }
+    if (top1) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, best, off);
-        const int oj = __shfl_xor_sync(0xffffffffu, bestj, off);
-        if (better(ov, oj, best, bestj)) {
-            best = ov;
-            bestj = oj;
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, best, off);
+            const int oj = __shfl_xor_sync(0xffffffffu, bestj, off);
+            if (better(ov, oj, best, bestj)) {
+                best = ov;
+                bestj = oj;
+            }
         }
-    }
-    if ((tid & 31) == 0) {
-        red_v[tid >> 5] = best;
-        red_j[tid >> 5] = bestj;
+        if ((tid & 31) == 0) {
+            red_v[tid >> 5] = best;
+            red_j[tid >> 5] = bestj;
+        }
+        consumer_bar_sync();
+        if (tid == 0) {
+            for (int w = 1; w < kConsumerWarps; ++w)
+                if (better(red_v[w], red_j[w], best, bestj)) {
+                    best = red_v[w];
+                    bestj = red_j[w];
+                }
+            const int slot = (bestj == 0x7fffffff) ? -1 : bestj;
+            p.next_slot[u] = slot;
+            if (slot >= 0 && (p.flags & kFlagMaskEvicted))
+                p.mask[static_cast<size_t>(u) * S + slot] = -1;
+        }
+    } else {
+        if (ncand) atomicAdd(s_ncand, ncand);
+        consumer_bar_sync();
+        select_topk(p, u, keys, G, s_ncand[0], topk_area, tid);
     }
     consumer_bar_sync();
-    if (tid == 0) {
-        for (int w = 1; w < kConsumerWarps; ++w)
-            if (better(red_v[w], red_j[w], best, bestj)) {
-                best = red_v[w];
-                bestj = red_j[w];
-            }
-        p.next_slot[u] = (bestj == 0x7fffffff) ? -1 : bestj;
-    }
-    // Every read of the unit's scratch is done: drop the lines, no write-back.
     discard_range(stash, static_cast<size_t>(S) * G * sizeof(float), tid, kConsumers);
-    discard_range(po, static_cast<size_t>(nchunk) * G * D * sizeof(float), tid, kConsumers);
+}
+
+// Shared-memory bytes finish_unit needs (it reuses the pipeline buffers).
+__host__ __device__ constexpr size_t finish_smem_bytes(int nchunk, int G, int topk) {
+    return (static_cast<size_t>(nchunk) * G + 2 * G + 2 * kConsumerWarps + 4) * 4 + 16 +
+           (topk > 1 ? (256 + 4) * 4 + 2 * static_cast<size_t>(kMaxTopK) * 4 : 0);
 }
 
 // kStages-deep TMA ring; 3 stages run 2 CTAs per SM, 2 stages run 3.
-template <int D, int G, int kStages>
+// kScore = false is the attention-only variant (no ageing, score or eviction).
+template <int D, int G, int kStages, bool kScore>
 __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
     lf_decode_step_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const StepParams p) {
@@ -330,7 +520,11 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
         if (i < n) {
             int a = av[k];
             if (ws >= 0) {
-                const int na = (slot0 + i == ws) ? 0 : ((a >= 0 && a != 0x7fffffff) ? a + 1 : a);
+                int na;
+                if constexpr (kScore)
+                    na = (slot0 + i == ws) ? 0 : ((a >= 0 && a != 0x7fffffff) ? a + 1 : a);
+                else
+                    na = (slot0 + i == ws && a < 0) ? 0 : a;  // the written slot is live
                 if (na != a) mrow[i] = na;
                 a = na;
             }
@@ -445,13 +639,16 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = swz_off(lrow, 2 * kk + (lane >> 4));
-                uint32_t a[4], v[4];
+                uint32_t a[4];
                 ldsm_x4(kbase + off, a);
-                ldsm_x4(vbase + off, v);
                 mma_bf16_16816(sc, a, qf[kk][0], qf[kk][1]);
+                if constexpr (kScore) {
+                    uint32_t v[4];
+                    ldsm_x4(vbase + off, v);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) v[e] &= kAbsBf16x2;
-                mma_bf16_16816(nv, v, kOnesBf16x2, kOnesBf16x2);
+                    for (int e = 0; e < 4; ++e) v[e] &= kAbsBf16x2;
+                    mma_bf16_16816(nv, v, kOnesBf16x2, kOnesBf16x2);
+                }
             }
         }
 
@@ -462,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
         const float x3 = (liveB && hv1) ? sc[3] * sl : NEG;
 
         // Per-slot score terms t = log2(exp(s) * ||v||_1).
-        if (hv0) {
+        if (kScore && hv0) {
             const int slotA = tslot0 + wrow0 + r;
             float* st = p.stash + (static_cast<size_t>(u) * S + slotA) * G + h0;
             if (liveA) {
@@ -611,47 +808,60 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
     consumer_bar_sync();
     if (!misc[2]) return;
     __threadfence();
-    finish_unit<D, G>(p, u, smem, tid);
+    finish_unit<D, G, kScore>(p, u, smem, tid);
 }
 
-template <int D, int G, int kStages>
+template <int D, int G, int kStages, bool kScore>
 cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
                      int units, cudaStream_t stream) {
     using L = StepSmem<D, kStages>;
+    if (finish_smem_bytes(p.nchunk, G, kScore ? p.topk : 1) > static_cast<size_t>(L::kBarOff))
+        return cudaErrorInvalidConfiguration;
     static int configured_for = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_for != dev) {
-        e = cudaFuncSetAttribute(lf_decode_step_kernel<D, G, kStages>,
+        e = cudaFuncSetAttribute(lf_decode_step_kernel<D, G, kStages, kScore>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
     dim3 grid(p.nchunk, units);
-    lf_decode_step_kernel<D, G, kStages><<<grid, kThreads, L::kAlloc, stream>>>(tmK, tmV, p);
+    lf_decode_step_kernel<D, G, kStages, kScore><<<grid, kThreads, L::kAlloc, stream>>>(tmK, tmV, p);
     return cudaGetLastError();
 }
 
 template <int D, int G>
 cudaError_t launch_dg(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
-                      int units, cudaStream_t stream, int stages) {
-    return stages == 2 ? launch_t<D, G, 2>(tmK, tmV, p, units, stream)
-                       : launch_t<D, G, 3>(tmK, tmV, p, units, stream);
+                      int units, cudaStream_t stream, int stages, bool score) {
+    if (!score) return launch_t<D, G, 2, false>(tmK, tmV, p, units, stream);
+    return stages == 2 ? launch_t<D, G, 2, true>(tmK, tmV, p, units, stream)
+                       : launch_t<D, G, 3, true>(tmK, tmV, p, units, stream);
 }
 
 }  // namespace
+
+bool step_fits(int D, int G, int stages, bool score, int nchunk, int topk) {
+    const size_t need = finish_smem_bytes(nchunk, G, score ? topk : 1);
+    size_t have;
+    if (stages == 2 || !score)
+        have = D == 64 ? StepSmem<64, 2>::kBarOff : StepSmem<128, 2>::kBarOff;
+    else
+        have = D == 64 ? StepSmem<64, 3>::kBarOff : StepSmem<128, 3>::kBarOff;
+    return need <= have;
+}
 
 size_t step_smem_bytes(int D, int stages) {
     if (stages == 2) return D == 64 ? StepSmem<64, 2>::kAlloc : StepSmem<128, 2>::kAlloc;
     return D == 64 ? StepSmem<64, 3>::kAlloc : StepSmem<128, 3>::kAlloc;
 }
 
-cudaError_t launch_decode_step(int D, int G, int stages, const CUtensorMap& tmK,
+cudaError_t launch_decode_step(int D, int G, int stages, bool score, const CUtensorMap& tmK,
                                const CUtensorMap& tmV, const StepParams& p, int units,
                                cudaStream_t stream) {
 #define LF_STEP_CASE(DD, GG) \
-    if (D == DD && G == GG) return launch_dg<DD, GG>(tmK, tmV, p, units, stream, stages);
+    if (D == DD && G == GG) return launch_dg<DD, GG>(tmK, tmV, p, units, stream, stages, score);
     LF_STEP_CASE(64, 1) LF_STEP_CASE(64, 2) LF_STEP_CASE(64, 4) LF_STEP_CASE(64, 8)
     LF_STEP_CASE(128, 1) LF_STEP_CASE(128, 2) LF_STEP_CASE(128, 4) LF_STEP_CASE(128, 8)
 #undef LF_STEP_CASE

@@ -25,7 +25,7 @@ struct StepParams {
     const __nv_bfloat16* new_v;  // [units][D]
     const int32_t* write_slot;   // [units]
     __nv_bfloat16* out;          // [B][Hq][D]
-    int32_t* next_slot;          // [units]
+    int32_t* next_slot;          // [units][topk] slots to overwrite, ascending (score, slot)
     float* scores;               // [units][S] or nullptr
     // scratch
     float* part_o;               // [units][nchunk][G][D]  unnormalised output, base m
@@ -35,13 +35,25 @@ struct StepParams {
     uint32_t* dev_err;           // LF_DEVERR_* bits
     int Hq, Hkv, S, W, nchunk, chunk_tiles;
     float scale_log2;            // scale * log2(e)
+    int topk;                    // slots returned per unit (1 = the argmin)
+    int flags;                   // kFlag* bits
 };
+
+constexpr int kFlagFillEmptyFirst = 1;  // empty (masked) slots are returned before any score
+constexpr int kFlagMaskEvicted = 2;     // returned slots are masked (-1) in place
+constexpr int kMaxTopK = 1024;
 
 // Dynamic shared memory the kernel needs for head dim D and a TMA ring of
 // `stages` tiles (2 or 3).
 size_t step_smem_bytes(int D, int stages);
 
-cudaError_t launch_decode_step(int D, int G, int stages, const CUtensorMap& tmK,
+// Whether finish-stage shared memory (chunk weights, top-k list) fits.
+bool step_fits(int D, int G, int stages, bool score, int nchunk, int topk);
+
+// score = false runs the attention-only variant: the slot write (the written
+// slot becomes live; no other age changes) and the attention output, without
+// LongFlowScore or eviction. next_slot, scores and topk are then unused.
+cudaError_t launch_decode_step(int D, int G, int stages, bool score, const CUtensorMap& tmK,
                                const CUtensorMap& tmV, const StepParams& p, int units,
                                cudaStream_t stream);
 

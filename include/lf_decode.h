@@ -74,8 +74,14 @@ typedef enum lf_status {
 #define LF_DEVERR_WAIT_TIMEOUT 0x2u   /* a pipeline wait gave up; that step's results are invalid */
 
 /* Kernel ids for lf_profile_collect. A decode step is one launch of one kernel. */
-#define LF_KERNEL_DECODE_STEP 0 /* slot write, mask ageing, attention, score, argmin */
-#define LF_KERNEL_COUNT 1
+#define LF_KERNEL_DECODE_STEP 0 /* slot write, mask ageing, attention, score, eviction */
+#define LF_KERNEL_ATTENTION 1   /* lf_decode_attention: slot write and attention only */
+#define LF_KERNEL_COUNT 2
+
+/* Flags of lf_decode_step_ex. */
+#define LF_STEP_FILL_EMPTY_FIRST 0x1 /* return empty (masked) slots, lowest first, before any score */
+#define LF_STEP_MASK_EVICTED 0x2     /* mask (-1) the returned slots in place */
+#define LF_MAX_TOPK 1024             /* largest k of lf_decode_step_ex */
 
 /*
  * One decode step (all three stages above) on device buffers.
@@ -108,6 +114,45 @@ lf_status lf_decode_step_scores(const void* q, void* k_cache, void* v_cache, int
                                 const int32_t* write_slot, void* out, int32_t* next_slot,
                                 float* scores, int B, int Hq, int Hkv, int d, int S, int W,
                                 float scale, void* stream);
+
+/*
+ * lf_decode_step with a choice of what to return.
+ *
+ * next_slots out int32 [B][Hkv][k]: the k candidates with the lowest
+ *     (LongFlowScore, slot) per unit, ascending; -1 past the last candidate.
+ *     k = 1 is lf_decode_step's argmin. Candidates are live slots with
+ *     age >= W, plus empty (masked) slots with LF_STEP_FILL_EMPTY_FIRST.
+ * k      1 <= k <= LF_MAX_TOPK. A k > 1 returns k slots at once: the
+ *        periodic compression that the paper's baselines run every 128 steps
+ *        (Fig. 3 caption), built on LongFlowScore instead of per-step argmin.
+ * flags  LF_STEP_FILL_EMPTY_FIRST: while a unit has empty slots, return them
+ *        (lowest index first) before any scored slot, i.e. fill the budget
+ *        before evicting (the cache-fill phase before the budget is full).
+ *        LF_STEP_MASK_EVICTED: set the mask of every returned slot to -1, so
+ *        it is not attended again until a later step writes into it.
+ * scores optional float [B][Hkv][S] as in lf_decode_step_scores (NULL = none).
+ * The other arguments are those of lf_decode_step. A combination of k and
+ * slot-axis split that does not fit in shared memory returns
+ * LF_ERR_UNSUPPORTED.
+ */
+lf_status lf_decode_step_ex(const void* q, void* k_cache, void* v_cache, int32_t* mask,
+                            const void* new_k, const void* new_v, const int32_t* write_slot,
+                            void* out, int32_t* next_slots, int k, int flags, float* scores,
+                            int B, int Hq, int Hkv, int d, int S, int W, float scale,
+                            void* stream);
+
+/*
+ * Decode attention alone, with the same kernel pipeline and no LongFlowScore:
+ * the current K/V row is written into write_slot (which becomes live with age
+ * 0 if it was empty; no other mask entry changes), then the g query heads of
+ * each unit attend over the mask-gated cache. No score, no eviction, no
+ * ageing. This is the baseline that measures what the score and eviction
+ * cost on top of attention (the abstract calls it negligible).
+ */
+lf_status lf_decode_attention(const void* q, void* k_cache, void* v_cache, int32_t* mask,
+                              const void* new_k, const void* new_v, const int32_t* write_slot,
+                              void* out, int B, int Hq, int Hkv, int d, int S, float scale,
+                              void* stream);
 
 /*
  * One decode step whose per-step inputs and outputs live in HOST memory, for

@@ -229,8 +229,8 @@ def bench_reference(args, wl):
     return 0
 
 
-def workload_config(wl, world):
-    return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d, "S": wl.S,
+def workload_config(wl, world, layers=1):
+    return {"workload": wl.name, "layers": layers, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d, "S": wl.S,
             "W": wl.W, "live": list(wl.live) if isinstance(wl.live, tuple) else wl.live,
             "description": wl.description,
             "l2": "inputs larger than L2 (K/V caches >> 129 MB); no flush between steps",
@@ -268,20 +268,45 @@ def bench_lf(args, wl):
         inp = step_inputs(wl, s, batch_offset=shard.batch_offset, full_batch=shard.full_batch)
         pool.append({kk: bf16_dev(vv, device) for kk, vv in inp.items()})
     out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.bfloat16, device=device)
-    slots = [torch.full((wl.B, wl.Hkv), -1, dtype=torch.int32, device=device),
-             torch.empty((wl.B, wl.Hkv), dtype=torch.int32, device=device)]
-    stream = torch.cuda.current_stream(device)
+    # Layer 0 holds the generated caches; further layers (--layers) are copies,
+    # each with its own mask and write/next slot pair.
+    L = args.layers
+    layers = [(k, v, mask)] + [(k.clone(), v.clone(), mask.clone()) for _ in range(L - 1)]
+    slots = [[torch.full((wl.B, wl.Hkv), -1, dtype=torch.int32, device=device),
+              torch.empty((wl.B, wl.Hkv), dtype=torch.int32, device=device)] for _ in range(L)]
+    use_graph = L > 1
+    stream = torch.cuda.Stream(device) if use_graph else torch.cuda.current_stream(device)
 
-    def step(i):
+    def step_eager(i, layer_ids=None):
         p = pool[i % len(pool)]
-        lf.decode_step(p["q"], k, v, mask, p["new_k"], p["new_v"], slots[i % 2], out,
-                       slots[(i + 1) % 2], wl.W, wl.scale, stream=stream)
+        for li in (range(L) if layer_ids is None else layer_ids):
+            kk, vv, mm = layers[li]
+            lf.decode_step(p["q"], kk, vv, mm, p["new_k"], p["new_v"], slots[li][i % 2], out,
+                           slots[li][(i + 1) % 2], wl.W, wl.scale, stream=stream)
 
-    for i in range(args.warmup):
-        step(i)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step_eager(i)
     torch.cuda.synchronize()
     if lf.device_errors(stream) != 0:
         raise RuntimeError("device error word set during warm-up")
+
+    graphs = []
+    if use_graph:
+        # One token through all L layers per replay; two graphs alternate the
+        # write/next slot buffers of every layer.
+        for parity in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step_eager(args.warmup + parity)
+            graphs.append(g)
+        torch.cuda.synchronize()
+
+    def step(i):
+        if use_graph:
+            graphs[i % 2].replay()
+        else:
+            step_eager(args.warmup + i)
 
     # ---------------------------------------------------------- device-timed
     clocks = ClockSampler(local)
@@ -292,20 +317,50 @@ def bench_lf(args, wl):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    lf.profile_enable(True)
+    lf.profile_enable(not use_graph)
     t_wall0 = clocks.mark()
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i)
-    ev1.record(stream)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = clocks.mark()
     lf.profile_enable(False)
     ms_total = ev0.elapsed_time(ev1)
-    kern_ms, kern_n = lf.profile_collect(lf.LF_KERNEL_DECODE_STEP)
+    if use_graph:
+        kern_ms, kern_n = ms_total, args.steps * L   # graph replays: launches back to back
+    else:
+        kern_ms, kern_n = lf.profile_collect(lf.LF_KERNEL_DECODE_STEP)
     ms_total = max_over_ranks(ms_total, device)
     if lf.device_errors(stream) != 0:
         raise RuntimeError("device error word set during the timed steps")
+
+    # ------------------------------------- score + eviction over attention
+    overhead = None
+    if not args.no_overhead:
+        n_o = max(20, min(args.steps, 200))
+        att_ws = slots[0][0].clone()
+        lf.profile_collect(lf.LF_KERNEL_ATTENTION)
+        lf.profile_collect(lf.LF_KERNEL_DECODE_STEP)
+        torch.cuda.synchronize()
+        lf.profile_enable(True)
+        with torch.cuda.stream(stream):
+            for i in range(n_o):
+                step_eager(i, layer_ids=[0])
+            for i in range(n_o):
+                p = pool[i % len(pool)]
+                lf.decode_attention(p["q"], k, v, mask, p["new_k"], p["new_v"], att_ws, out,
+                                    wl.scale, stream=stream)
+        torch.cuda.synchronize()
+        lf.profile_enable(False)
+        f_ms, f_n = lf.profile_collect(lf.LF_KERNEL_DECODE_STEP)
+        a_ms, a_n = lf.profile_collect(lf.LF_KERNEL_ATTENTION)
+        f_avg, a_avg = f_ms / max(f_n, 1), a_ms / max(a_n, 1)
+        overhead = {"fused_kernel_ms": f_avg, "attention_only_kernel_ms": a_avg,
+                    "frac": (f_avg - a_avg) / a_avg if a_avg > 0 else None, "launches": n_o,
+                    "how": "same resident caches; lf_decode_step vs lf_decode_attention "
+                           "(same pipeline without row norms, score terms, ageing, selection)"}
 
     # ------------------------------------------------------ end to end (host)
     pin = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
@@ -314,15 +369,17 @@ def bench_lf(args, wl):
         inp = step_inputs(wl, s, batch_offset=shard.batch_offset, full_batch=shard.full_batch)
         hpool.append({kk: pin(vv).view(torch.bfloat16) for kk, vv in inp.items()})
     h_out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.bfloat16).pin_memory()
-    h_ws = torch.full((wl.B, wl.Hkv), -1, dtype=torch.int32).pin_memory()
-    h_next = torch.empty((wl.B, wl.Hkv), dtype=torch.int32).pin_memory()
+    h_ws = [torch.full((wl.B, wl.Hkv), -1, dtype=torch.int32).pin_memory() for _ in range(L)]
+    h_next = [torch.empty((wl.B, wl.Hkv), dtype=torch.int32).pin_memory() for _ in range(L)]
 
     def e2e_step(i):
         p = hpool[i % len(hpool)]
-        lf.decode_step_host(p["q"], k, v, mask, p["new_k"], p["new_v"], h_ws, h_out, h_next,
-                            wl.W, wl.scale, stream=stream)
+        for li, (kk, vv, mm) in enumerate(layers):
+            lf.decode_step_host(p["q"], kk, vv, mm, p["new_k"], p["new_v"], h_ws[li], h_out,
+                                h_next[li], wl.W, wl.scale, stream=stream)
         stream.synchronize()
-        h_ws.copy_(h_next)
+        for li in range(L):
+            h_ws[li].copy_(h_next[li])
 
     for i in range(min(args.warmup, 5)):
         e2e_step(i)
@@ -334,8 +391,8 @@ def bench_lf(args, wl):
     e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, device)
     clocks.stop()
-    h2d = (wl.B * wl.Hq * wl.d * 2) + 2 * (wl.B * wl.Hkv * wl.d * 2) + wl.B * wl.Hkv * 4
-    d2h = wl.B * wl.Hq * wl.d * 2 + wl.B * wl.Hkv * 4
+    h2d = L * ((wl.B * wl.Hq * wl.d * 2) + 2 * (wl.B * wl.Hkv * wl.d * 2) + wl.B * wl.Hkv * 4)
+    d2h = L * (wl.B * wl.Hq * wl.d * 2 + wl.B * wl.Hkv * 4)
 
     # ------------------------------------------------------------ CPU oracle
     cpu = None
@@ -343,20 +400,21 @@ def bench_lf(args, wl):
         import oracle
         oracle.build()
         n, secs, threads = run_oracle_steps(wl, host, max_seconds=args.cpu_seconds, max_steps=50)
-        cpu = {"value": n / secs, "unit": "steps/s", "cores": threads, "kind": "oracle",
-               "sample": f"{n} full decode step(s) of the same workload, fp64, "
-                         f"{threads} OpenMP threads"}
+        cpu = {"value": n / secs / L, "unit": "steps/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} full decode step(s) of one layer of the same workload, fp64, "
+                         f"{threads} OpenMP threads" + (f", divided by {L} layers" if L > 1 else "")}
 
     if rank != 0:
         return 0
 
     ms_per_step = ms_total / args.steps
     value = world * args.steps / (ms_total / 1e3)
-    alg = algorithmic_bytes(wl, lengths)
+    alg_launch = algorithmic_bytes(wl, lengths)
+    alg = alg_launch * L
     kern_avg_ms = kern_ms / max(kern_n, 1)
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    achieved = alg / (kern_avg_ms / 1e3) / 1e9
+    achieved = alg_launch / (kern_avg_ms / 1e3) / 1e9
     step_gbs = alg / (ms_per_step / 1e3) / 1e9
     line = {
         "metric": METRIC,
@@ -371,19 +429,24 @@ def bench_lf(args, wl):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": workload_config(wl, world),
+        "config": workload_config(wl, world, L),
         "hbm": {"algorithmic_bytes_per_step": alg, "achieved_gbs": step_gbs,
                 "frac_of_measured_peak": step_gbs / peak, "frac_of_8000_gbs": step_gbs / 8000.0,
                 "peak_kind": peak_kind},
         "roofline": {"kernel": "lf_decode_step_kernel", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": committed_traffic(), "algorithmic_bytes_per_launch": alg,
+                     "traffic": committed_traffic() if L == 1 else None,
+                     "algorithmic_bytes_per_launch": alg_launch,
                      "avg_launch_ms": kern_avg_ms, "launches": kern_n,
+                     "timing": "library CUDA events per launch" if not use_graph else
+                               "CUDA-graph replay time / launches",
                      "peak_source": f"{peak_kind} hbm_gbs"},
+        "overhead_vs_attention_only": overhead,
         "cpu_baseline": cpu,
         "e2e": {"value": world * args.steps / e2e_s, "unit": "steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "lf_decode_step_host from pinned host buffers; stream sync every step"},
+                "how": "lf_decode_step_host per layer from pinned host buffers; "
+                       "stream sync every step"},
         "gpu_launches": kern_n,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
@@ -406,6 +469,11 @@ def main():
                     help="(b,kvh) units the reference arm runs per step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-overhead", action="store_true",
+                    help="skip the attention-only comparison")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="decode through L layers' caches per step (one CUDA graph per "
+                         "token when L > 1); Qwen3-8B has 36")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps, always
     wl = WORKLOADS[args.workload]

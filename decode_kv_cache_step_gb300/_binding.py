@@ -60,12 +60,15 @@ def library_path() -> str:
 
 
 def load_library(path: str | None = None):
-    """Load (once) and bind the shared library. Raises if it is missing."""
+    """Load (once) and bind the shared library. Raises if it is missing.
+
+    The environment variable LF_LIBRARY names another build of the same
+    library (for comparing two builds in one session)."""
     global _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
-        p = path or _build.LIB_PATH
+        p = path or os.environ.get("LF_LIBRARY") or _build.LIB_PATH
         if not os.path.exists(p):
             raise RuntimeError(
                 f"{p} is missing: build it first with "

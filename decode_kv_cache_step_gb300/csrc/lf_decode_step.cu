@@ -65,12 +65,27 @@ struct StepSmem {
     static constexpr int kListOff = kAgesOff + kAgesBytes;
     static constexpr int kMiscOff = kListOff + kMaxChunkTiles * 4;
     static constexpr int kBarOff = kMiscOff + 16;
-    static constexpr int kBytes = kBarOff + 2 * kStages * 8;
+    static constexpr int kScanBarOff = kBarOff + 2 * kStages * 8;  // the finish's 2 barriers
+    static constexpr int kBytes = kScanBarOff + 16;
     static constexpr int kAlloc = kBytes + 1024;               // slack for 1024-B alignment
 };
 
 __device__ __forceinline__ void consumer_bar_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+// Consumer barrier that also returns whether any consumer passed `pred`.
+__device__ __forceinline__ bool consumer_bar_or(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "n"(kConsumers)
+        : "memory");
+    return r != 0;
 }
 
 // Byte offset of 16-byte chunk `cg` (8 bf16 columns) of tile row `row` in a
@@ -154,6 +169,9 @@ __device__ __forceinline__ int radix_pass(const uint32_t* keys, int stride, int 
     *digit_out = static_cast<uint32_t>(s_out[0]);
     return s_out[1];
 }
+
+// Shared memory of select_topk: histogram, scalars, the winners' keys and slots.
+constexpr int kTopKAreaBytes = (256 + 4) * 4 + 2 * kMaxTopK * 4;
 
 // The k smallest (key, slot) pairs of a unit, ascending, into next_slot[u][k]
 // (-1 past the number of candidates). Keys were written one per slot (stride
@@ -246,12 +264,15 @@ __device__ void select_topk(const StepParams& p, int u, const uint32_t* keys, in
 
 template <int G>
 __device__ void score_and_select(const StepParams& p, int u, const float* s_m, const float* s_il,
-                                 float* red_v, int* red_j, int* s_ncand, uint8_t* topk_area,
-                                 int tid);
+                                 float* red_v, int* red_j, int* s_ncand, const int* s_live,
+                                 uint8_t* topk_area, uint8_t* scan_area, int scan_bytes,
+                                 uint64_t* scan_bars, int tid);
 
-// Merge of the unit's chunks by its last CTA (consumer threads only).
+// Merge of the unit's chunks by its last CTA (consumer threads only). The
+// shared memory below `usable` is free; scan_bars are two spare mbarriers.
 template <int D, int G, bool kScore>
-__device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) {
+__device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int usable,
+                            uint64_t* scan_bars, int tid) {
     const int nchunk = p.nchunk;
     float* s_w = reinterpret_cast<float*>(smem);  // [nchunk][G]: 2^(m_c - m) / l
     float* s_m = s_w + nchunk * G;                // [G]
@@ -259,8 +280,11 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) 
     float* red_v = s_il + G;                      // [4]
     int* red_j = reinterpret_cast<int*>(red_v + kConsumerWarps);
     int* s_ncand = red_j + kConsumerWarps;
+    int* s_live = s_ncand + 4;                    // [nchunk]: 1 if the chunk has a live slot
     uint8_t* topk_area = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(s_ncand + 4) + 15) & ~static_cast<uintptr_t>(15));
+        (reinterpret_cast<uintptr_t>(s_live + nchunk) + 15) & ~static_cast<uintptr_t>(15));
+    uint8_t* scan_area = topk_area + (p.topk > 1 ? kTopKAreaBytes : 0);
+    const int scan_bytes = usable - static_cast<int>(scan_area - smem);
     const float2* ml = p.part_ml + static_cast<size_t>(u) * nchunk * G;
 
     if (tid < G) {
@@ -280,6 +304,7 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) 
         const float2 v = __ldcg(&ml[e]);
         const int h = e % G;
         s_w[e] = (v.x == -INFINITY) ? 0.f : exp2f(v.x - s_m[h]) * s_il[h];
+        if (h == 0) s_live[e / G] = v.x != -INFINITY;  // m = -inf: no live slot
     }
     consumer_bar_sync();
 
@@ -322,28 +347,68 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int tid) 
         const int e = tid + k * kConsumers;
         if (e < G * D) out[e] = __float2bfloat16_rn(o[k]);
     }
-    if constexpr (kScore) score_and_select<G>(p, u, s_m, s_il, red_v, red_j, s_ncand, topk_area, tid);
+    if constexpr (kScore)
+        score_and_select<G>(p, u, s_m, s_il, red_v, red_j, s_ncand, s_live, topk_area, scan_area,
+                            scan_bytes, scan_bars, tid);
     consumer_bar_sync();
     // Every read of the unit's scratch is done: drop the lines, no write-back.
     discard_range(po, static_cast<size_t>(nchunk) * G * D * sizeof(float), tid, kConsumers);
 }
 
+// Segments of a unit's slot axis that the score scan visits, in order: pieces
+// of at most `seg` slots of the runs of consecutive chunks that hold a live
+// slot (of all chunks when `all` is set). The same walk runs in every
+// consumer thread.
+struct SegWalk {
+    int j0;    // first slot of the current segment (>= S: done)
+    int rend;  // end of the current run of chunks
+};
+
+__device__ __forceinline__ int next_chunk(int c, int nchunk, const int* s_live, bool all) {
+    while (c < nchunk && !(all || s_live[c])) ++c;
+    return c;
+}
+
+// Starts a run at chunk c (or ends the walk when c == nchunk).
+__device__ __forceinline__ SegWalk seg_run(int c, int cs, int S, int nchunk, const int* s_live,
+                                           bool all) {
+    if (c >= nchunk) return SegWalk{S, S};
+    int e = c;
+    while (e + 1 < nchunk && (all || s_live[e + 1])) ++e;
+    return SegWalk{c * cs, min((e + 1) * cs, S)};
+}
+
+__device__ __forceinline__ int seg_end(const SegWalk& w, int seg) { return min(w.j0 + seg, w.rend); }
+
+__device__ __forceinline__ void seg_advance(SegWalk& w, int cs, int seg, int S, int nchunk,
+                                            const int* s_live, bool all) {
+    const int e = seg_end(w, seg);
+    if (e < w.rend)
+        w.j0 = e;
+    else
+        w = seg_run(next_chunk((w.rend + cs - 1) / cs, nchunk, s_live, all), cs, S, nchunk,
+                    s_live, all);
+}
+
+// Units with more slots to score than this stream them through shared memory.
+constexpr int kBulkScanMinSlots = 4096;
+
 // LongFlowScore of every live slot of unit u and the selection of the slots to
 // evict, by the unit's last CTA once the final (m_h, l_h) are known.
 template <int G>
 __device__ void score_and_select(const StepParams& p, int u, const float* s_m, const float* s_il,
-                                 float* red_v, int* red_j, int* s_ncand, uint8_t* topk_area,
-                                 int tid) {
-    // LongFlowScore of every live slot; selection over the candidates: live
-    // slots with age >= W and, with kFlagFillEmptyFirst, empty slots (ranked
-    // before every score, lowest slot first).
-    float m[G], il[G];
+                                 float* red_v, int* red_j, int* s_ncand, const int* s_live,
+                                 uint8_t* topk_area, uint8_t* scan_area, int scan_bytes,
+                                 uint64_t* scan_bars, int tid) {
+    // Candidates: live slots with age >= W and, with kFlagFillEmptyFirst,
+    // empty slots (ranked before every score, lowest slot first).
+    // I_j = sum_h 2^(t_hj - m_h) / l_h = sum_h 2^(t_hj + c_h), c_h = log2(1/l_h) - m_h.
+    float c[G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m[h] = s_m[h];
-        il[h] = s_il[h];
-    }
+    for (int h = 0; h < G; ++h) c[h] = __log2f(s_il[h]) - s_m[h];
     const int S = p.S;
+    const int nchunk = p.nchunk;
+    const int cs = p.chunk_tiles * kTile;
     const int32_t* age = p.mask + static_cast<size_t>(u) * S;
     float* stash = p.stash + static_cast<size_t>(u) * S * G;
     // For top-k the slot's first stash word is reused for its selection key.
@@ -351,55 +416,155 @@ __device__ void score_and_select(const StepParams& p, int u, const float* s_m, c
     float* scores = p.scores ? p.scores + static_cast<size_t>(u) * S : nullptr;
     const bool fill_first = (p.flags & kFlagFillEmptyFirst) != 0;
     const bool top1 = p.topk == 1;
+    // Chunks without a live slot hold no scored candidate; they are visited
+    // only when empty slots are candidates or every score is wanted.
+    const bool all = fill_first || scores != nullptr;
     float best = INFINITY;
     int bestj = 0x7fffffff;
     int ncand = 0;
-    // Batches of kBatch slots per thread: all loads of a batch are in flight
-    // together instead of one L2 round trip per slot.
-    constexpr int kBatch = 8;
-    for (int j0 = tid; j0 < S; j0 += kBatch * kConsumers) {
-        int a[kBatch];
-        float t[kBatch][G];
+
+    auto visit = [&](int j, int a, const float* t) {
+        float I = INFINITY;
+        bool cand = false;
+        float cval = 0.f;
+        if (a >= 0) {
+            I = 0.f;
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            const int j = j0 + k * kConsumers;
-            a[k] = (j < S) ? __ldcg(&age[j]) : -1;
+            for (int h = 0; h < G; ++h) I += ex2_approx(t[h] + c[h]);
+            cand = a >= p.W && !isnan(I);
+            cval = I;
+        } else if (fill_first) {
+            cand = true;
+            cval = -1.f;
         }
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            const int j = j0 + k * kConsumers;
-            if (j < S) load_terms<G>(stash + static_cast<size_t>(j) * G, t[k]);
-        }
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            const int j = j0 + k * kConsumers;
-            if (j >= S) break;
-            float I = INFINITY;
-            bool cand = false;
-            float cval = 0.f;
-            if (a[k] >= 0) {
-                I = 0.f;
-#pragma unroll
-                for (int h = 0; h < G; ++h) I += exp2f(t[k][h] - m[h]) * il[h];
-                cand = a[k] >= p.W && !isnan(I);
-                cval = I;
-            } else if (fill_first) {
-                cand = true;
-                cval = -1.f;
+        if (top1) {
+            if (cand && better(cval, j, best, bestj)) {
+                best = cval;
+                bestj = j;
             }
-            if (top1) {
-                if (cand && better(cval, j, best, bestj)) {
-                    best = cval;
-                    bestj = j;
+        } else {
+            keys[static_cast<size_t>(j) * G] =
+                !cand ? 0xffffffffu : (cval < 0.f ? 0u : __float_as_uint(cval) + 1u);
+            ncand += cand ? 1 : 0;
+        }
+        if (scores) scores[j] = I;
+    };
+
+    if (!all && !top1) {
+        // Top-k reads a key for every slot: skipped chunks hold no candidate.
+        for (int c = 0; c < nchunk; ++c)
+            if (!s_live[c])
+                for (int j = c * cs + tid; j < min(S, (c + 1) * cs); j += kConsumers)
+                    keys[static_cast<size_t>(j) * G] = 0xffffffffu;
+    }
+
+    // A long scan streams each segment's ages and score terms into shared memory
+    // with bulk copies, two segments in flight, so it runs at L2 bandwidth
+    // instead of one round trip per slot.
+    constexpr int kSlotBytes = (G + 1) * 4;
+    int seg = (scan_bytes / 2) / kSlotBytes;
+    seg = min(2048, seg & ~(kConsumers - 1));
+    // Short units are cheaper with loads batched in registers (one or two
+    // round trips); long ones stream through shared memory.
+    int nlive = 0;
+    for (int c = 0; c < nchunk; ++c) nlive += (all || s_live[c]) ? 1 : 0;
+    const bool bulk = seg >= kConsumers && nlive * cs > kBulkScanMinSlots && (S & 3) == 0 &&
+                      (reinterpret_cast<uintptr_t>(p.mask) & 15) == 0;
+    if (bulk) {
+        const int half = seg * kSlotBytes;
+        uint8_t* buf0 = reinterpret_cast<uint8_t*>(
+            (reinterpret_cast<uintptr_t>(scan_area) + 15) & ~static_cast<uintptr_t>(15));
+        if (tid == 0) {
+            mbar_init(&scan_bars[0], 1);
+            mbar_init(&scan_bars[1], 1);
+            fence_barrier_init();
+            // The ages and score terms were written through the generic proxy
+            // (here and by the unit's other CTAs); the copies read them through
+            // the async proxy.
+            asm volatile("fence.proxy.async;" ::: "memory");
+        }
+        consumer_bar_sync();
+        SegWalk wi = seg_run(next_chunk(0, nchunk, s_live, all), cs, S, nchunk, s_live, all);
+        SegWalk wc = wi;
+        int issued = 0;
+        auto issue = [&](int s_idx) {
+            const int j1 = seg_end(wi, seg);
+            const int n = j1 - wi.j0;
+            uint8_t* b = buf0 + (s_idx & 1) * half;
+            uint64_t* bar = &scan_bars[s_idx & 1];
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * kSlotBytes));
+            bulk_load(b, age + wi.j0, static_cast<uint32_t>(n * 4), bar);
+            bulk_load(b + seg * 4, stash + static_cast<size_t>(wi.j0) * G,
+                      static_cast<uint32_t>(n * G * 4), bar);
+            seg_advance(wi, cs, seg, S, nchunk, s_live, all);
+        };
+        if (tid == 0) {
+            for (; issued < 2 && wi.j0 < S; ++issued) issue(issued);
+        }
+        int s_idx = 0;
+        for (; wc.j0 < S; ++s_idx) {
+            const int b = s_idx & 1;
+            const bool timed_out = !mbar_wait(&scan_bars[b], (s_idx >> 1) & 1);
+            if (consumer_bar_or(timed_out)) {
+                if (tid == 0) {
+                    atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
+                    // Copies still in flight land before the CTA retires.
+                    for (int q = s_idx; q < issued; ++q)
+                        (void)mbar_wait(&scan_bars[q & 1], (q >> 1) & 1);
                 }
-            } else {
-                keys[static_cast<size_t>(j) * G] =
-                    !cand ? 0xffffffffu : (cval < 0.f ? 0u : __float_as_uint(cval) + 1u);
-                ncand += cand ? 1 : 0;
+                break;
             }
-            if (scores) scores[j] = I;
+            const int32_t* s_age = reinterpret_cast<const int32_t*>(buf0 + b * half);
+            const float* s_t = reinterpret_cast<const float*>(buf0 + b * half + seg * 4);
+            const int n = seg_end(wc, seg) - wc.j0;
+#pragma unroll 4
+            for (int i = tid; i < n; i += kConsumers) {
+                float t[G];
+                if constexpr (G >= 4) {
+#pragma unroll
+                    for (int q4 = 0; q4 < G / 4; ++q4) {
+                        const float4 v = reinterpret_cast<const float4*>(s_t + i * G)[q4];
+                        t[4 * q4] = v.x;
+                        t[4 * q4 + 1] = v.y;
+                        t[4 * q4 + 2] = v.z;
+                        t[4 * q4 + 3] = v.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) t[h] = s_t[i * G + h];
+                }
+                visit(wc.j0 + i, s_age[i], t);
+            }
+            consumer_bar_sync();  // everyone is done with buffer b
+            if (tid == 0 && wi.j0 < S) issue(issued++);
+            seg_advance(wc, cs, seg, S, nchunk, s_live, all);
+        }
+    } else {
+        // Batches of loads in flight per thread (also for slot counts that
+        // break the 16-byte copy alignment).
+        constexpr int kBatch = 8;
+        for (int j0 = tid; j0 < S; j0 += kBatch * kConsumers) {
+            int a[kBatch];
+            float t[kBatch][G];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int j = j0 + k * kConsumers;
+                a[k] = (j < S) ? __ldcg(&age[j]) : -1;
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int j = j0 + k * kConsumers;
+                if (j < S) load_terms<G>(stash + static_cast<size_t>(j) * G, t[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int j = j0 + k * kConsumers;
+                if (j >= S) break;
+                visit(j, a[k], t[k]);  // a slot of a chunk with no live slot is no candidate
+            }
         }
     }
+
     if (top1) {
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -437,8 +602,8 @@ __device__ void score_and_select(const StepParams& p, int u, const float* s_m, c
 
 // Shared-memory bytes finish_unit needs (it reuses the pipeline buffers).
 __host__ __device__ constexpr size_t finish_smem_bytes(int nchunk, int G, int topk) {
-    return (static_cast<size_t>(nchunk) * G + 2 * G + 2 * kConsumerWarps + 4) * 4 + 16 +
-           (topk > 1 ? (256 + 4) * 4 + 2 * static_cast<size_t>(kMaxTopK) * 4 : 0);
+    return (static_cast<size_t>(nchunk) * (G + 1) + 2 * G + 2 * kConsumerWarps + 4) * 4 + 16 +
+           (topk > 1 ? kTopKAreaBytes : 0);
 }
 
 // kStages-deep TMA ring; 3 stages run 2 CTAs per SM, 2 stages run 3.
@@ -808,7 +973,8 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
     consumer_bar_sync();
     if (!misc[2]) return;
     __threadfence();
-    finish_unit<D, G, kScore>(p, u, smem, tid);
+    finish_unit<D, G, kScore>(p, u, smem, L::kBarOff,
+                              reinterpret_cast<uint64_t*>(smem + L::kScanBarOff), tid);
 }
 
 template <int D, int G, int kStages, bool kScore>

@@ -185,6 +185,16 @@ lf_status encode_cache_map(CUtensorMap* m, void* base, int D, int S, int units) 
     return LF_OK;
 }
 
+// Limit of the kernel's pipeline waits: 1 s, or LF_WAIT_LIMIT_NS (a
+// diagnostic that makes the waits give up early, to exercise the timeout path).
+uint64_t wait_limit_ns() {
+    if (const char* env = std::getenv("LF_WAIT_LIMIT_NS")) {
+        const long long v = std::atoll(env);
+        if (v > 0) return static_cast<uint64_t>(v);
+    }
+    return 1000000000ull;
+}
+
 // ---------------------------------------------------------------- planning --
 
 struct Plan {
@@ -335,6 +345,7 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
     sp.nchunk = pl.nchunk;
     sp.chunk_tiles = pl.chunk_tiles;
     sp.scale_log2 = static_cast<float>(static_cast<double>(s.scale) * 1.4426950408889634);
+    sp.wait_limit_ns = wait_limit_ns();
     sp.topk = a.score ? a.topk : 1;
     sp.flags = a.score ? a.flags : 0;
     if (!lf::step_fits(s.d, g, pl.stages, a.score, pl.nchunk, sp.topk))
@@ -545,6 +556,7 @@ lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, in
     g_last_error[0] = '\0';
     sp.topk = 1;
     sp.flags = 0;
+    sp.wait_limit_ns = wait_limit_ns();
     e = lf::launch_decode_step(d, g, pl.stages, true, tmK, tmV, sp, static_cast<int>(units), stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");
     return LF_OK;

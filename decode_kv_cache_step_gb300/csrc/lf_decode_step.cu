@@ -504,7 +504,7 @@ __device__ void score_and_select(const StepParams& p, int u, const float* s_m, c
         int s_idx = 0;
         for (; wc.j0 < S; ++s_idx) {
             const int b = s_idx & 1;
-            const bool timed_out = !mbar_wait(&scan_bars[b], (s_idx >> 1) & 1);
+            const bool timed_out = !mbar_wait(&scan_bars[b], (s_idx >> 1) & 1, p.wait_limit_ns);
             if (consumer_bar_or(timed_out)) {
                 if (tid == 0) {
                     atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
@@ -724,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
             int issued = 0;
             for (int i = 0; i < cnt; ++i) {
                 const int s = i % kStages;
-                if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1)) {
+                if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, p.wait_limit_ns)) {
                     atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
                     misc[1] = 1;
                     break;
@@ -762,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
 
     for (int i = 0; i < cnt; ++i) {
         const int s = i % kStages;
-        if (!mbar_wait(&full[s], (i / kStages) & 1)) {
+        if (!mbar_wait(&full[s], (i / kStages) & 1, p.wait_limit_ns)) {
             if (lane == 0) atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
             misc[1] = 1;
             break;

@@ -37,6 +37,8 @@ struct StepParams {
     float scale_log2;            // scale * log2(e)
     int topk;                    // slots returned per unit (1 = the argmin)
     int flags;                   // kFlag* bits
+    // Limit of the pipeline waits; drains of copies in flight always allow 1 s.
+    uint64_t wait_limit_ns;
 };
 
 constexpr int kFlagFillEmptyFirst = 1;  // empty (masked) slots are returned before any score

@@ -199,6 +199,7 @@ uint64_t wait_limit_ns() {
 
 struct Plan {
     int tiles, chunk_tiles, nchunk, stages;
+    bool cluster;  // the unit's chunks run as one thread-block cluster
 };
 
 // Split the slot axis of every unit into nchunk chunks of chunk_tiles tiles.
@@ -207,7 +208,7 @@ struct Plan {
 // balance the tail; a batch too small to fill the GPU that way uses short
 // chunks of about 5 tiles instead. At most kMaxChunkTiles tiles and
 // kMaxNChunk chunks.
-Plan plan_split(int S, int units, int sms) {
+Plan plan_split(int S, int units, int sms, bool want_cluster) {
     Plan pl;
     pl.tiles = (S + lf::kTile - 1) / lf::kTile;
     int nchunk = 0;
@@ -229,6 +230,25 @@ Plan plan_split(int S, int units, int sms) {
     pl.nchunk = (pl.tiles + pl.chunk_tiles - 1) / pl.chunk_tiles;
     pl.stages = 2;
     if (const char* env = std::getenv("LF_STAGES")) pl.stages = (std::atoi(env) == 3) ? 3 : 2;
+    // A grid that fits in one wave (3 CTAs per SM) of units of at most
+    // kMaxClusterChunks chunks merges inside thread-block clusters: the
+    // latency-bound small batches gain the shorter merge. Larger grids keep
+    // the last-CTA merge, where a finished CTA frees its slot at once instead
+    // of waiting for its cluster. LF_CLUSTER=0 turns clusters off, =1 forces
+    // them whenever the shape allows.
+    pl.cluster = false;
+    const char* cenv = std::getenv("LF_CLUSTER");
+    const int cmode = cenv ? std::atoi(cenv) : -1;
+    const bool one_wave = static_cast<long>(units) *
+                              std::min(pl.nchunk, lf::kMaxClusterChunks) <= 3L * sms;
+    if (want_cluster && pl.stages == 2 && cmode != 0 && (cmode == 1 || one_wave) &&
+        pl.tiles <= lf::kMaxClusterChunks * lf::kMaxChunkTiles) {
+        if (pl.nchunk > lf::kMaxClusterChunks) {
+            pl.chunk_tiles = (pl.tiles + lf::kMaxClusterChunks - 1) / lf::kMaxClusterChunks;
+            pl.nchunk = (pl.tiles + pl.chunk_tiles - 1) / pl.chunk_tiles;
+        }
+        pl.cluster = true;
+    }
     return pl;
 }
 
@@ -356,7 +376,14 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
     cudaError_t e;
     {
         ProfScope prof(a.score ? LF_KERNEL_DECODE_STEP : LF_KERNEL_ATTENTION, stream);
-        e = lf::launch_decode_step(s.d, g, pl.stages, a.score, tmK, tmV, sp, units, stream);
+        const bool cluster = pl.cluster && sp.topk == 1;
+        e = lf::launch_decode_step(s.d, g, pl.stages, a.score, cluster, tmK, tmV, sp, units, stream);
+        if (e != cudaSuccess && cluster) {
+            // A cluster that cannot be scheduled: the last-CTA merge instead.
+            (void)cudaGetLastError();
+            e = lf::launch_decode_step(s.d, g, pl.stages, a.score, false, tmK, tmV, sp, units,
+                                       stream);
+        }
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");
     return LF_OK;
@@ -369,7 +396,7 @@ lf_status run_step(const StepArgs& a, const Shape& s, void* stream_v) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    const Plan pl = plan_split(s.S, s.B * s.Hkv, sm_count(dev));
+    const Plan pl = plan_split(s.S, s.B * s.Hkv, sm_count(dev), a.topk == 1);
     const Layout L = scratch_layout(s, pl, 0);
     Scratch* scr = nullptr;
     if ((st = get_scratch(dev, stream, L.total, static_cast<size_t>(s.B) * s.Hkv, &scr)) != LF_OK) return st;
@@ -473,7 +500,7 @@ lf_status lf_decode_step_host(const void* q_host, void* k_cache, void* v_cache, 
     size_t off_q = 0, off_k = align_up(off_q + q_bytes, 256), off_v = align_up(off_k + kv_bytes, 256),
            off_w = align_up(off_v + kv_bytes, 256), off_o = align_up(off_w + i_bytes, 256),
            off_n = align_up(off_o + q_bytes, 256), staging = align_up(off_n + i_bytes, 256);
-    const Plan pl = plan_split(S, static_cast<int>(units), sm_count(dev));
+    const Plan pl = plan_split(S, static_cast<int>(units), sm_count(dev), true);
     const Layout L = scratch_layout(s, pl, staging);
     Scratch* scr = nullptr;
     if ((st = get_scratch(dev, stream, L.total, static_cast<size_t>(s.B) * s.Hkv, &scr)) != LF_OK) return st;
@@ -509,7 +536,7 @@ lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, in
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return cuda_fail(e, "cudaDeviceGetAttribute");
     const size_t units = static_cast<size_t>(B) * Hkv;
-    const Plan pl = plan_split(S, static_cast<int>(units), sms > 0 ? sms : 1);
+    const Plan pl = plan_split(S, static_cast<int>(units), sms > 0 ? sms : 1, true);
     const Layout L = scratch_layout(s, pl, 0);
     const size_t arrivals_off = align_up(L.total, 256);
     const size_t err_off = align_up(arrivals_off + units * sizeof(uint32_t), 256);
@@ -557,7 +584,13 @@ lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, in
     sp.topk = 1;
     sp.flags = 0;
     sp.wait_limit_ns = wait_limit_ns();
-    e = lf::launch_decode_step(d, g, pl.stages, true, tmK, tmV, sp, static_cast<int>(units), stream);
+    e = lf::launch_decode_step(d, g, pl.stages, true, pl.cluster, tmK, tmV, sp,
+                               static_cast<int>(units), stream);
+    if (e != cudaSuccess && pl.cluster) {
+        (void)cudaGetLastError();
+        e = lf::launch_decode_step(d, g, pl.stages, true, false, tmK, tmV, sp,
+                                   static_cast<int>(units), stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");
     return LF_OK;
 }

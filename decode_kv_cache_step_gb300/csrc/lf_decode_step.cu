@@ -606,9 +606,207 @@ __host__ __device__ constexpr size_t finish_smem_bytes(int nchunk, int G, int to
            (topk > 1 ? kTopKAreaBytes : 0);
 }
 
+// Epilogue when the unit's chunks run as one thread-block cluster (rank =
+// chunk). The chunk's merged (m, l, O) stay in shared memory; after a
+// cluster barrier every CTA reads its peers' through distributed shared
+// memory. CTA r writes its slice of the output row, every CTA scores only
+// its own chunk's slots, and rank 0 reduces the cluster's (I_j, j) argmin.
+// wO/wm/wl hold the four consumer warps' states (consumer threads only; the
+// producer warp joins the three cluster barriers on its own).
+template <int D, int G, bool kScore>
+__device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
+                                 const int32_t* ages, uint8_t* smem, const float* wO,
+                                 const float* wm, const float* wl, int cnt, int tid) {
+    const int nchunk = p.nchunk;
+    const uint32_t rank = cluster_ctarank();
+    constexpr int kWBytes = (kConsumerWarps * G * D + 2 * kConsumerWarps * G) * 4;
+    float* pub_o = reinterpret_cast<float*>(smem + ((kWBytes + 15) & ~15));  // [G][D]
+    float2* pub_ml = reinterpret_cast<float2*>(pub_o + G * D);               // [G]
+    float* pub_best = reinterpret_cast<float*>(pub_ml + G);                  // [1]
+    int* pub_bestj = reinterpret_cast<int*>(pub_best + 1);                   // [1]
+    float2* s_mlc = reinterpret_cast<float2*>(pub_bestj + 3);                // [nchunk][G]
+    float* s_w = reinterpret_cast<float*>(s_mlc + kMaxClusterChunks * G);    // [nchunk][G]
+    float* s_m = s_w + kMaxClusterChunks * G;                               // [G]
+    float* s_il = s_m + G;                                                   // [G]
+    float* red_v = s_il + G;                                                 // [4]
+    int* red_j = reinterpret_cast<int*>(red_v + kConsumerWarps);             // [4]
+    const float NEG = -INFINITY;
+
+    // This chunk's merged state, published for the cluster.
+    for (int e = tid; e < G * D; e += kConsumers) {
+        const int h = e / D;
+        float mh = NEG;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) mh = fmaxf(mh, wm[w * G + h]);
+        float o = 0.f;
+        if (cnt > 0) {
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float mw = wm[w * G + h];
+                if (mw != NEG) o += wO[w * G * D + e] * exp2f(mw - mh);
+            }
+        }
+        pub_o[e] = o;
+    }
+    if (tid < G) {
+        float mh = NEG, l = 0.f;
+        if (cnt > 0) {
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) mh = fmaxf(mh, wm[w * G + tid]);
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float mw = wm[w * G + tid];
+                if (mw != NEG) l += wl[w * G + tid] * exp2f(mw - mh);
+            }
+        } else {
+            mh = NEG;
+        }
+        pub_ml[tid] = make_float2(mh, l);
+    }
+    cluster_sync();  // #1: every chunk's state is published
+
+    for (int e = tid; e < nchunk * G; e += kConsumers) {
+        const uint32_t a = dsmem_addr(&pub_ml[e % G], static_cast<uint32_t>(e / G));
+        s_mlc[e] = make_float2(ld_dsmem_f32(a), ld_dsmem_f32(a + 4));
+    }
+    consumer_bar_sync();
+    if (tid < G) {
+        float m = NEG;
+        for (int c = 0; c < nchunk; ++c) m = fmaxf(m, s_mlc[c * G + tid].x);
+        float l = 0.f;
+        for (int c = 0; c < nchunk; ++c) {
+            const float2 v = s_mlc[c * G + tid];
+            if (v.x != NEG) l += v.y * exp2f(v.x - m);
+        }
+        s_m[tid] = m;
+        s_il[tid] = (l > 0.f) ? 1.f / l : 0.f;
+    }
+    consumer_bar_sync();
+    for (int e = tid; e < nchunk * G; e += kConsumers) {
+        const float2 v = s_mlc[e];
+        const int h = e % G;
+        s_w[e] = (v.x == NEG) ? 0.f : exp2f(v.x - s_m[h]) * s_il[h];
+    }
+    consumer_bar_sync();
+
+    // This CTA's slice of the output row: O_h = sum_c w_ch * O_ch.
+    {
+        const int b = u / p.Hkv;
+        const int kvh = u - b * p.Hkv;
+        __nv_bfloat16* out = p.out + (static_cast<size_t>(b) * p.Hq + kvh * G) * D;
+        const int per = (G * D + nchunk - 1) / nchunk;
+        const int e0 = static_cast<int>(rank) * per;
+        const int e1 = min(G * D, e0 + per);
+        for (int e = e0 + tid; e < e1; e += kConsumers) {
+            const int h = e / D;
+            float o = 0.f;
+            for (int c = 0; c < nchunk; ++c) {
+                const float w = s_w[c * G + h];
+                const float v = ld_dsmem_f32(dsmem_addr(&pub_o[e], static_cast<uint32_t>(c)));
+                o += (w != 0.f) ? w * v : 0.f;
+            }
+            out[e] = __float2bfloat16_rn(o);
+        }
+    }
+
+    if constexpr (kScore) {
+        // LongFlowScore of this chunk's slots and their local best candidate.
+        float cexp[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) cexp[h] = __log2f(s_il[h]) - s_m[h];
+        const int S = p.S;
+        const float* stash = p.stash + static_cast<size_t>(u) * S * G;
+        float* scores = p.scores ? p.scores + static_cast<size_t>(u) * S : nullptr;
+        const bool fill_first = (p.flags & kFlagFillEmptyFirst) != 0;
+        float best = INFINITY;
+        int bestj = 0x7fffffff;
+        constexpr int kBatch = 8;
+        for (int i0 = tid; i0 < n; i0 += kBatch * kConsumers) {
+            float t[kBatch][G];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int i = i0 + k * kConsumers;
+                if (i < n && ages[i] >= 0)
+                    load_terms<G>(stash + static_cast<size_t>(slot0 + i) * G, t[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int i = i0 + k * kConsumers;
+                if (i >= n) break;
+                const int a = ages[i];
+                const int j = slot0 + i;
+                float I = INFINITY;
+                bool cand = false;
+                float cval = 0.f;
+                if (a >= 0) {
+                    I = 0.f;
+#pragma unroll
+                    for (int h = 0; h < G; ++h) I += ex2_approx(t[k][h] + cexp[h]);
+                    cand = a >= p.W && !isnan(I);
+                    cval = I;
+                } else if (fill_first) {
+                    cand = true;
+                    cval = -1.f;
+                }
+                if (cand && better(cval, j, best, bestj)) {
+                    best = cval;
+                    bestj = j;
+                }
+                if (scores) scores[j] = I;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, best, off);
+            const int oj = __shfl_xor_sync(0xffffffffu, bestj, off);
+            if (better(ov, oj, best, bestj)) {
+                best = ov;
+                bestj = oj;
+            }
+        }
+        if ((tid & 31) == 0) {
+            red_v[tid >> 5] = best;
+            red_j[tid >> 5] = bestj;
+        }
+        consumer_bar_sync();
+        if (tid == 0) {
+            for (int w = 1; w < kConsumerWarps; ++w)
+                if (better(red_v[w], red_j[w], best, bestj)) {
+                    best = red_v[w];
+                    bestj = red_j[w];
+                }
+            *pub_best = best;
+            *pub_bestj = bestj;
+        }
+        // This chunk's score terms are read: drop them from L2, no write-back.
+        discard_range(stash + static_cast<size_t>(slot0) * G, static_cast<size_t>(n) * G * 4, tid,
+                      kConsumers);
+    }
+    cluster_sync();  // #2: every output slice is written, every local best published
+
+    if (kScore && rank == 0 && tid == 0) {
+        float best = INFINITY;
+        int bestj = 0x7fffffff;
+        for (int c = 0; c < nchunk; ++c) {
+            const float v = ld_dsmem_f32(dsmem_addr(pub_best, static_cast<uint32_t>(c)));
+            const int j = ld_dsmem_s32(dsmem_addr(pub_bestj, static_cast<uint32_t>(c)));
+            if (better(v, j, best, bestj)) {
+                best = v;
+                bestj = j;
+            }
+        }
+        const int slot = (bestj == 0x7fffffff) ? -1 : bestj;
+        p.next_slot[u] = slot;
+        if (slot >= 0 && (p.flags & kFlagMaskEvicted))
+            p.mask[static_cast<size_t>(u) * p.S + slot] = -1;
+    }
+    cluster_sync();  // #3: no CTA leaves while a peer may still read its memory
+}
+
 // kStages-deep TMA ring; 3 stages run 2 CTAs per SM, 2 stages run 3.
 // kScore = false is the attention-only variant (no ageing, score or eviction).
-template <int D, int G, int kStages, bool kScore>
+// kCluster: the grid is launched in clusters of nchunk CTAs (one per unit).
+template <int D, int G, int kStages, bool kScore, bool kCluster>
 __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
     lf_decode_step_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const StepParams p) {
@@ -744,6 +942,12 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
             // Every issued copy has landed before the CTA may retire.
             for (int i = max(0, issued - kStages); i < issued; ++i)
                 (void)mbar_wait(&full[i % kStages], (i / kStages) & 1);
+        }
+        if constexpr (kCluster) {
+            __syncwarp();
+            cluster_sync();  // the consumers' cluster barriers #1, #2, #3
+            cluster_sync();
+            cluster_sync();
         }
         return;
     }
@@ -926,6 +1130,11 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
     }
     consumer_bar_sync();
 
+    if constexpr (kCluster) {
+        cluster_epilogue<D, G, kScore>(p, u, slot0, n, ages, smem, wO, wm, wl, cnt, tid);
+        return;
+    }
+
     const size_t pidx = static_cast<size_t>(u) * p.nchunk + chunk;
     if (cnt > 0) {
         float* po = p.part_o + pidx * G * D;
@@ -977,33 +1186,53 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
                               reinterpret_cast<uint64_t*>(smem + L::kScanBarOff), tid);
 }
 
-template <int D, int G, int kStages, bool kScore>
+template <int D, int G, int kStages, bool kScore, bool kCluster>
 cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
                      int units, cudaStream_t stream) {
     using L = StepSmem<D, kStages>;
     if (finish_smem_bytes(p.nchunk, G, kScore ? p.topk : 1) > static_cast<size_t>(L::kBarOff))
         return cudaErrorInvalidConfiguration;
+    auto kernel = lf_decode_step_kernel<D, G, kStages, kScore, kCluster>;
     static int configured_for = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_for != dev) {
-        e = cudaFuncSetAttribute(lf_decode_step_kernel<D, G, kStages, kScore>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
     dim3 grid(p.nchunk, units);
-    lf_decode_step_kernel<D, G, kStages, kScore><<<grid, kThreads, L::kAlloc, stream>>>(tmK, tmV, p);
+    if constexpr (kCluster) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = L::kAlloc;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(p.nchunk);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kernel, tmK, tmV, p);
+        if (e != cudaSuccess) return e;
+    } else {
+        kernel<<<grid, kThreads, L::kAlloc, stream>>>(tmK, tmV, p);
+    }
     return cudaGetLastError();
 }
 
 template <int D, int G>
 cudaError_t launch_dg(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
-                      int units, cudaStream_t stream, int stages, bool score) {
-    if (!score) return launch_t<D, G, 2, false>(tmK, tmV, p, units, stream);
-    return stages == 2 ? launch_t<D, G, 2, true>(tmK, tmV, p, units, stream)
-                       : launch_t<D, G, 3, true>(tmK, tmV, p, units, stream);
+                      int units, cudaStream_t stream, int stages, bool score, bool cluster) {
+    if (cluster)
+        return score ? launch_t<D, G, 2, true, true>(tmK, tmV, p, units, stream)
+                     : launch_t<D, G, 2, false, true>(tmK, tmV, p, units, stream);
+    if (!score) return launch_t<D, G, 2, false, false>(tmK, tmV, p, units, stream);
+    return stages == 2 ? launch_t<D, G, 2, true, false>(tmK, tmV, p, units, stream)
+                       : launch_t<D, G, 3, true, false>(tmK, tmV, p, units, stream);
 }
 
 }  // namespace
@@ -1023,11 +1252,12 @@ size_t step_smem_bytes(int D, int stages) {
     return D == 64 ? StepSmem<64, 3>::kAlloc : StepSmem<128, 3>::kAlloc;
 }
 
-cudaError_t launch_decode_step(int D, int G, int stages, bool score, const CUtensorMap& tmK,
-                               const CUtensorMap& tmV, const StepParams& p, int units,
-                               cudaStream_t stream) {
+cudaError_t launch_decode_step(int D, int G, int stages, bool score, bool cluster,
+                               const CUtensorMap& tmK, const CUtensorMap& tmV,
+                               const StepParams& p, int units, cudaStream_t stream) {
 #define LF_STEP_CASE(DD, GG) \
-    if (D == DD && G == GG) return launch_dg<DD, GG>(tmK, tmV, p, units, stream, stages, score);
+    if (D == DD && G == GG)  \
+        return launch_dg<DD, GG>(tmK, tmV, p, units, stream, stages, score, cluster);
     LF_STEP_CASE(64, 1) LF_STEP_CASE(64, 2) LF_STEP_CASE(64, 4) LF_STEP_CASE(64, 8)
     LF_STEP_CASE(128, 1) LF_STEP_CASE(128, 2) LF_STEP_CASE(128, 4) LF_STEP_CASE(128, 8)
 #undef LF_STEP_CASE

@@ -44,6 +44,7 @@ struct StepParams {
 constexpr int kFlagFillEmptyFirst = 1;  // empty (masked) slots are returned before any score
 constexpr int kFlagMaskEvicted = 2;     // returned slots are masked (-1) in place
 constexpr int kMaxTopK = 1024;
+constexpr int kMaxClusterChunks = 8;    // chunks of a unit run as one cluster up to this
 
 // Dynamic shared memory the kernel needs for head dim D and a TMA ring of
 // `stages` tiles (2 or 3).
@@ -55,8 +56,11 @@ bool step_fits(int D, int G, int stages, bool score, int nchunk, int topk);
 // score = false runs the attention-only variant: the slot write (the written
 // slot becomes live; no other age changes) and the attention output, without
 // LongFlowScore or eviction. next_slot, scores and topk are then unused.
-cudaError_t launch_decode_step(int D, int G, int stages, bool score, const CUtensorMap& tmK,
-                               const CUtensorMap& tmV, const StepParams& p, int units,
-                               cudaStream_t stream);
+// cluster = true launches each unit's nchunk (<= kMaxClusterChunks) CTAs as
+// one thread-block cluster that merges through distributed shared memory
+// (2-stage ring, topk == 1 only); otherwise the unit's last CTA merges.
+cudaError_t launch_decode_step(int D, int G, int stages, bool score, bool cluster,
+                               const CUtensorMap& tmK, const CUtensorMap& tmV,
+                               const StepParams& p, int units, cudaStream_t stream);
 
 }  // namespace lf

@@ -40,6 +40,7 @@
 // An attention-only instantiation (kScore = false) drops the row norms, the
 // score terms, the ageing and the selection: the baseline for the overhead.
 #include <math.h>
+#include <stdlib.h>
 
 #include "../../include/lf_decode.h"
 #include "lf_kernels.h"
@@ -832,12 +833,6 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
     const int n = slot_end - slot0;
     const int ntiles = (n + kTile - 1) / kTile;
 
-    int ws = p.write_slot[u];
-    if (ws < -1 || ws >= S) {
-        if (tid == 0 && chunk == 0) atomicOr(p.dev_err, LF_DEVERR_BAD_WRITE_SLOT);
-        ws = -1;
-    }
-
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -845,6 +840,19 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
         }
         misc[1] = 0;
         fence_barrier_init();
+    }
+    // With programmatic dependent launch this CTA may start while the previous
+    // kernel of the stream (often the previous decode step) is still running:
+    // everything above touches only this CTA's shared memory; every global
+    // read comes after the wait. The next step may begin launching as soon as
+    // every CTA of this one has started.
+    allow_dependent_launch();
+    grid_dependency_wait();
+
+    int ws = p.write_slot[u];
+    if (ws < -1 || ws >= S) {
+        if (tid == 0 && chunk == 0) atomicOr(p.dev_err, LF_DEVERR_BAD_WRITE_SLOT);
+        ws = -1;
     }
 
     // Q^T as the B operand of S^T = K . Q^T, loaded early so its latency
@@ -1188,7 +1196,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
 
 template <int D, int G, int kStages, bool kScore, bool kCluster>
 cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
-                     int units, cudaStream_t stream) {
+                     int units, cudaStream_t stream, bool pdl) {
     using L = StepSmem<D, kStages>;
     if (finish_smem_bytes(p.nchunk, G, kScore ? p.topk : 1) > static_cast<size_t>(L::kBarOff))
         return cudaErrorInvalidConfiguration;
@@ -1202,37 +1210,42 @@ cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepP
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
-    dim3 grid(p.nchunk, units);
-    if constexpr (kCluster) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = grid;
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = L::kAlloc;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(p.nchunk);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kernel, tmK, tmV, p);
-        if (e != cudaSuccess) return e;
-    } else {
-        kernel<<<grid, kThreads, L::kAlloc, stream>>>(tmK, tmV, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.nchunk, units);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
     }
+    if constexpr (kCluster) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = static_cast<unsigned>(p.nchunk);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    e = cudaLaunchKernelEx(&cfg, kernel, tmK, tmV, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 template <int D, int G>
 cudaError_t launch_dg(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
-                      int units, cudaStream_t stream, int stages, bool score, bool cluster) {
+                      int units, cudaStream_t stream, int stages, bool score, bool cluster,
+                      bool pdl) {
     if (cluster)
-        return score ? launch_t<D, G, 2, true, true>(tmK, tmV, p, units, stream)
-                     : launch_t<D, G, 2, false, true>(tmK, tmV, p, units, stream);
-    if (!score) return launch_t<D, G, 2, false, false>(tmK, tmV, p, units, stream);
-    return stages == 2 ? launch_t<D, G, 2, true, false>(tmK, tmV, p, units, stream)
-                       : launch_t<D, G, 3, true, false>(tmK, tmV, p, units, stream);
+        return score ? launch_t<D, G, 2, true, true>(tmK, tmV, p, units, stream, pdl)
+                     : launch_t<D, G, 2, false, true>(tmK, tmV, p, units, stream, pdl);
+    if (!score) return launch_t<D, G, 2, false, false>(tmK, tmV, p, units, stream, pdl);
+    return stages == 2 ? launch_t<D, G, 2, true, false>(tmK, tmV, p, units, stream, pdl)
+                       : launch_t<D, G, 3, true, false>(tmK, tmV, p, units, stream, pdl);
 }
 
 }  // namespace
@@ -1255,9 +1268,13 @@ size_t step_smem_bytes(int D, int stages) {
 cudaError_t launch_decode_step(int D, int G, int stages, bool score, bool cluster,
                                const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const StepParams& p, int units, cudaStream_t stream) {
+    // Programmatic dependent launch overlaps this step's launch and set-up
+    // with the tail of the previous kernel in the stream (LF_PDL=0: off).
+    const char* env = std::getenv("LF_PDL");
+    const bool pdl = !(env && std::atoi(env) == 0);
 #define LF_STEP_CASE(DD, GG) \
     if (D == DD && G == GG)  \
-        return launch_dg<DD, GG>(tmK, tmV, p, units, stream, stages, score, cluster);
+        return launch_dg<DD, GG>(tmK, tmV, p, units, stream, stages, score, cluster, pdl);
     LF_STEP_CASE(64, 1) LF_STEP_CASE(64, 2) LF_STEP_CASE(64, 4) LF_STEP_CASE(64, 8)
     LF_STEP_CASE(128, 1) LF_STEP_CASE(128, 2) LF_STEP_CASE(128, 4) LF_STEP_CASE(128, 8)
 #undef LF_STEP_CASE

@@ -130,6 +130,20 @@ __device__ __forceinline__ void discard_l2_line(const void* p) {
     asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
 
+// --------------------------------------------- programmatic dependent launch --
+
+// Lets the next kernel in the stream start launching (its CTAs still wait in
+// grid_dependency_wait until this grid has completed). No-op without PDL.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grids this one depends on have completed and their memory
+// is visible. No-op when the kernel was not launched with PDL.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------ thread-block cluster --
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

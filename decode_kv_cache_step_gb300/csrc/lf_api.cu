@@ -2,6 +2,7 @@
 // split planning, scratch management, TMA descriptors and launches.
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>  // header-only; ranges are free unless a profiler is attached
 
 #include <algorithm>
 #include <cmath>
@@ -375,6 +376,11 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
 
     cudaError_t e;
     {
+        // A named range around each launch for timeline profilers (nsys).
+        struct NvtxRange {
+            explicit NvtxRange(const char* n) { nvtxRangePushA(n); }
+            ~NvtxRange() { nvtxRangePop(); }
+        } range(a.score ? "lf_decode_step" : "lf_decode_attention");
         ProfScope prof(a.score ? LF_KERNEL_DECODE_STEP : LF_KERNEL_ATTENTION, stream);
         const bool cluster = pl.cluster && sp.topk == 1;
         e = lf::launch_decode_step(s.d, g, pl.stages, a.score, cluster, tmK, tmV, sp, units, stream);

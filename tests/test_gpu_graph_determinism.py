@@ -1,0 +1,94 @@
+"""Two properties a serving loop relies on: a decode step captured in a CUDA
+graph (with its programmatic-dependent-launch edges) does exactly what the
+eager calls do, and a step is deterministic: the same resident state and
+inputs give the same bits, whichever launch path is taken (PDL on or off,
+cluster merge or last-CTA merge), so a snapshot of (caches, mask, slot) can be
+replayed."""
+import numpy as np
+import pytest
+import torch
+
+import decode_kv_cache_step_gb300 as lf
+from decode_kv_cache_step_gb300.workloads import WORKLOADS, initial_state, step_inputs
+
+from _gpu import to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _state(st):
+    return {"k": to_dev(st["k_cache"]), "v": to_dev(st["v_cache"]), "mask": to_dev(st["mask"])}
+
+
+def _two_steps(wl, state, inputs, stream, ws0, nxt1, nxt2, out):
+    for i, (ws, nx) in enumerate(((ws0, nxt1), (nxt1, nxt2))):
+        p = inputs[i]
+        lf.decode_step(p["q"], state["k"], state["v"], state["mask"], p["new_k"], p["new_v"], ws,
+                       out, nx, wl.W, wl.scale, stream=stream)
+
+
+@pytest.mark.parametrize("name", ["qwen3_8b_b1_s2400", "llama8b_b256_s2400_ragged"])
+def test_cuda_graph_replay_equals_eager(name):
+    wl = WORKLOADS[name]
+    if wl.B > 16:
+        wl = wl.with_batch(16)
+    st = initial_state(wl)
+    inputs = [{k: to_dev(v) for k, v in step_inputs(wl, t).items()} for t in range(2)]
+    shape = (wl.B, wl.Hkv)
+    mk = lambda: torch.empty(shape, dtype=torch.int32, device="cuda")
+    ws0 = torch.full(shape, -1, dtype=torch.int32, device="cuda")
+
+    eager = _state(st)
+    e1, e2 = mk(), mk()
+    out_e = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.bfloat16, device="cuda")
+    _two_steps(wl, eager, inputs, torch.cuda.current_stream(), ws0, e1, e2, out_e)
+    torch.cuda.synchronize()
+
+    s = torch.cuda.Stream()
+    graph_state = _state(st)
+    g1, g2 = mk(), mk()
+    out_g = torch.empty_like(out_e)
+    # Scratch for the capture stream is allocated by a call outside capture.
+    scratch_warm = _state(st)
+    with torch.cuda.stream(s):
+        _two_steps(wl, scratch_warm, inputs, s, ws0, mk(), mk(), torch.empty_like(out_e))
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        _two_steps(wl, graph_state, inputs, s, ws0, g1, g2, out_g)
+    # Capture records without running: restore the starting state, then replay.
+    graph_state["k"].copy_(to_dev(st["k_cache"]))
+    graph_state["v"].copy_(to_dev(st["v_cache"]))
+    graph_state["mask"].copy_(to_dev(st["mask"]))
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(g1, e1) and torch.equal(g2, e2)
+    assert torch.equal(out_g, out_e)
+    assert torch.equal(graph_state["mask"], eager["mask"])
+    assert torch.equal(graph_state["k"], eager["k"]) and torch.equal(graph_state["v"], eager["v"])
+    assert lf.device_errors(s) == 0
+
+
+@pytest.mark.parametrize("env", [{}, {"LF_PDL": "0"}, {"LF_CLUSTER": "0"}, {"LF_CLUSTER": "1"},
+                                 {"LF_STAGES": "3"}])
+def test_step_is_bitwise_deterministic(monkeypatch, env):
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    wl = WORKLOADS["qwen3_8b_b128_s3200"].with_batch(4)
+    st = initial_state(wl)
+    inp = {k: to_dev(v) for k, v in step_inputs(wl, 5).items()}
+    ws = to_dev(np.random.default_rng(5).integers(0, wl.S, size=(wl.B, wl.Hkv)).astype(np.int32))
+    results = []
+    for _ in range(2):
+        s = _state(st)
+        out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.bfloat16, device="cuda")
+        nxt = torch.empty((wl.B, wl.Hkv), dtype=torch.int32, device="cuda")
+        scores = torch.empty((wl.B, wl.Hkv, wl.S), dtype=torch.float32, device="cuda")
+        lf.decode_step_scores(inp["q"], s["k"], s["v"], s["mask"], inp["new_k"], inp["new_v"], ws,
+                              out, nxt, scores, wl.W, wl.scale)
+        torch.cuda.synchronize()
+        results.append((out, nxt, scores, s["mask"]))
+    a, b = results
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and torch.equal(a[3], b[3])
+    assert torch.equal(a[2], b[2])

@@ -370,6 +370,36 @@ def bench_lf(args, wl):
                     "how": "same resident caches; lf_decode_step vs lf_decode_attention "
                            "(same pipeline without row norms, score terms, ageing, selection)"}
 
+        # Per-token cost of two eviction policies on the same caches, back to
+        # back steps (events around each loop only): LongFlow's eviction at
+        # every step against compressing every K = 128 steps (K - 1 steps of
+        # attention alone, then one step returning and masking K slots).
+        K = 128
+        n_p = 2 * K
+        topk_out = torch.empty((wl.B, wl.Hkv, K), dtype=torch.int32, device=device)
+        pe = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        with torch.cuda.stream(stream):
+            pe[0].record(stream)
+            for i in range(n_p):
+                step_eager(i, layer_ids=[0])
+            pe[1].record(stream)
+            for i in range(n_p):
+                p = pool[i % len(pool)]
+                if i % K == K - 1:
+                    lf.decode_step_ex(p["q"], k, v, mask, p["new_k"], p["new_v"], att_ws, out,
+                                      topk_out, wl.W, wl.scale, k=K,
+                                      flags=lf.LF_STEP_MASK_EVICTED, stream=stream)
+                else:
+                    lf.decode_attention(p["q"], k, v, mask, p["new_k"], p["new_v"], att_ws, out,
+                                        wl.scale, stream=stream)
+            pe[2].record(stream)
+        torch.cuda.synchronize()
+        every = pe[0].elapsed_time(pe[1]) / n_p
+        periodic = pe[1].elapsed_time(pe[2]) / n_p
+        overhead["policy_ms_per_step"] = {
+            "every_step_argmin": every, f"every_{K}_steps_top{K}": periodic,
+            "frac": (every - periodic) / periodic if periodic > 0 else None}
+
     # ------------------------------------------------------ end to end (host)
     pin = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
     hpool = []

@@ -48,10 +48,17 @@ KERNEL_SOURCES = ["lf_decode_step.cu", "lf_ptx.cuh", "lf_kernels.h"]
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel's sources with comments and blank lines removed, so
+    that the committed ncu counters stay tied to the code, not its comments."""
+    import re
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "decode_kv_cache_step_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "decode_kv_cache_step_gb300", "csrc", name)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        text = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(text.encode())
     return h.hexdigest()[:16]
 
 

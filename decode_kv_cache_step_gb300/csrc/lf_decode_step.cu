@@ -18,8 +18,9 @@
 // Grid (nchunk, units). CTA (c, u) owns chunk c (up to 32 tiles of 64 slots)
 // of unit u = (b, kvh):
 //   warp 4, lane 0 : producer. TMA-loads the K and V tiles of the chunk's
-//                    live tiles (128-byte swizzled boxes, 3-stage mbarrier
-//                    ring, L2 evict-first: each byte is read once per step).
+//                    live tiles (128-byte swizzled boxes, 2- or 3-stage
+//                    mbarrier ring, L2 evict-first: each byte is read once
+//                    per step).
 //   warps 0..3     : consumers. Warp w owns rows 16w..16w+15 of every tile
 //                    and keeps its own online-softmax state. Per 16 slots:
 //        S^T[16 x 8]  = K[16 x D] . Q^T[D x 8]       (mma m16n8k16, heads as N)
@@ -37,8 +38,15 @@
 // index among equal scores) and a bitonic sort of the k winners; the periodic
 // k-at-once compression of the Fig. 3 caption. Empty slots can rank first
 // (cache-fill phase) and the chosen slots can be masked in place.
+// Long units stream their score terms through shared memory with bulk copies
+// for that scan. When the whole grid fits in one wave, a unit's chunks run as
+// one thread-block cluster instead (kCluster): they merge through distributed
+// shared memory and each CTA scores its own chunk (top-1 only).
 // An attention-only instantiation (kScore = false) drops the row norms, the
 // score terms, the ageing and the selection: the baseline for the overhead.
+// Launches use programmatic dependent launch: a CTA lets the next kernel of
+// the stream start launching as soon as it starts, and waits for the previous
+// one before its first global read.
 #include <math.h>
 #include <stdlib.h>
 

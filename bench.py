@@ -291,10 +291,20 @@ def bench_lf(args, wl):
             lf.decode_step(p["q"], kk, vv, mm, p["new_k"], p["new_v"], slots[li][i % 2], out,
                            slots[li][(i + 1) % 2], wl.W, wl.scale, stream=stream)
 
+    lf.profile_collect(lf.LF_KERNEL_DECODE_STEP)
+    lf.profile_collect(lf.LF_KERNEL_SCORE)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
+            if i == args.warmup - 1:
+                lf.profile_enable(True)   # count the kernels of one step
             step_eager(i)
     torch.cuda.synchronize()
+    lf.profile_enable(False)
+    n_step = lf.profile_collect(lf.LF_KERNEL_DECODE_STEP)[1]
+    n_score = lf.profile_collect(lf.LF_KERNEL_SCORE)[1]
+    # Kernel launches per layer step: the decode-step kernel, plus the
+    # scoring kernel when the step takes the split finish (long units).
+    launches_per_layer = 1 + (n_score // max(n_step, 1))
     if lf.device_errors(stream) != 0:
         raise RuntimeError("device error word set during warm-up")
 
@@ -319,6 +329,7 @@ def bench_lf(args, wl):
     clocks = ClockSampler(local)
     time.sleep(0.3)
     lf.profile_collect(lf.LF_KERNEL_DECODE_STEP)
+    lf.profile_collect(lf.LF_KERNEL_SCORE)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -336,6 +347,7 @@ def bench_lf(args, wl):
     ms_total = ev0.elapsed_time(ev1)
     # Pass 2 (roofline): K more steps with the library's CUDA events around
     # every launch, on the launching stream, for the kernel's own duration.
+    score_ms = 0.0
     if use_graph:
         kern_ms, kern_n = ms_total, args.steps * L   # graph replays: launches back to back
     else:
@@ -346,6 +358,7 @@ def bench_lf(args, wl):
         torch.cuda.synchronize()
         lf.profile_enable(False)
         kern_ms, kern_n = lf.profile_collect(lf.LF_KERNEL_DECODE_STEP)
+        score_ms = lf.profile_collect(lf.LF_KERNEL_SCORE)[0]
     t_wall1 = clocks.mark()
     ms_total = max_over_ranks(ms_total, device)
     if lf.device_errors(stream) != 0:
@@ -358,6 +371,7 @@ def bench_lf(args, wl):
         att_ws = slots[0][0].clone()
         lf.profile_collect(lf.LF_KERNEL_ATTENTION)
         lf.profile_collect(lf.LF_KERNEL_DECODE_STEP)
+        lf.profile_collect(lf.LF_KERNEL_SCORE)
         torch.cuda.synchronize()
         lf.profile_enable(True)
         with torch.cuda.stream(stream):
@@ -370,12 +384,16 @@ def bench_lf(args, wl):
         torch.cuda.synchronize()
         lf.profile_enable(False)
         f_ms, f_n = lf.profile_collect(lf.LF_KERNEL_DECODE_STEP)
+        fs_ms = lf.profile_collect(lf.LF_KERNEL_SCORE)[0]
         a_ms, a_n = lf.profile_collect(lf.LF_KERNEL_ATTENTION)
-        f_avg, a_avg = f_ms / max(f_n, 1), a_ms / max(a_n, 1)
+        f_avg, a_avg = (f_ms + fs_ms) / max(f_n, 1), a_ms / max(a_n, 1)
         overhead = {"fused_kernel_ms": f_avg, "attention_only_kernel_ms": a_avg,
                     "frac": (f_avg - a_avg) / a_avg if a_avg > 0 else None, "launches": n_o,
-                    "how": "same resident caches; lf_decode_step vs lf_decode_attention "
-                           "(same pipeline without row norms, score terms, ageing, selection)"}
+                    "score_kernel_ms": fs_ms / max(f_n, 1),
+                    "how": "same resident caches; lf_decode_step (its kernels, the scoring "
+                           "kernel included when the step splits its finish) vs "
+                           "lf_decode_attention (same pipeline without row norms, score terms, "
+                           "ageing, selection)"}
 
         # Per-token cost of two eviction policies on the same caches, back to
         # back steps (events around each loop only): LongFlow's eviction at
@@ -456,7 +474,10 @@ def bench_lf(args, wl):
     value = world * args.steps / (ms_total / 1e3)
     alg_launch = algorithmic_bytes(wl, lengths)
     alg = alg_launch * L
-    kern_avg_ms = kern_ms / max(kern_n, 1)
+    # A split finish adds the scoring kernel to every step: the roofline then
+    # covers both kernels of the step (their summed event times).
+    split = launches_per_layer > 1
+    kern_avg_ms = (kern_ms + score_ms) / max(kern_n, 1)
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     achieved = alg_launch / (kern_avg_ms / 1e3) / 1e9
@@ -478,11 +499,13 @@ def bench_lf(args, wl):
         "hbm": {"algorithmic_bytes_per_step": alg, "achieved_gbs": step_gbs,
                 "frac_of_measured_peak": step_gbs / peak, "frac_of_8000_gbs": step_gbs / 8000.0,
                 "peak_kind": peak_kind},
-        "roofline": {"kernel": "lf_decode_step_kernel", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": "lf_decode_step_kernel" + (" + lf_score_kernel" if split else ""),
+                     "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": committed_traffic() if L == 1 else None,
+                     "traffic": committed_traffic() if L == 1 and not split else None,
                      "algorithmic_bytes_per_launch": alg_launch,
                      "avg_launch_ms": kern_avg_ms, "launches": kern_n,
+                     "score_kernel_avg_ms": score_ms / max(kern_n, 1) if split else None,
                      "timing": ("library CUDA events around each launch, second timed pass "
                                 "of K steps") if not use_graph else
                                "CUDA-graph replay time / launches",
@@ -493,7 +516,7 @@ def bench_lf(args, wl):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "lf_decode_step_host per layer from pinned host buffers; "
                        "stream sync every step"},
-        "gpu_launches": args.steps * L,
+        "gpu_launches": args.steps * L * launches_per_layer,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
     print(json.dumps(line), flush=True)

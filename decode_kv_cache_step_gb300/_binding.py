@@ -27,8 +27,10 @@ LF_DEVERR_WAIT_TIMEOUT = 0x2
 
 LF_KERNEL_DECODE_STEP = 0
 LF_KERNEL_ATTENTION = 1
+LF_KERNEL_SCORE = 2
 KERNEL_NAMES = {LF_KERNEL_DECODE_STEP: "lf_decode_step_kernel",
-                LF_KERNEL_ATTENTION: "lf_decode_step_kernel (attention-only variant)"}
+                LF_KERNEL_ATTENTION: "lf_decode_step_kernel (attention-only variant)",
+                LF_KERNEL_SCORE: "lf_score_kernel"}
 
 LF_STEP_FILL_EMPTY_FIRST = 0x1
 LF_STEP_MASK_EVICTED = 0x2

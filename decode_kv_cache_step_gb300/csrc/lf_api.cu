@@ -48,7 +48,10 @@ struct Scratch {
     void* base = nullptr;
     size_t bytes = 0;
     uint32_t* dev_err = nullptr;   // never moves once created
-    uint32_t* arrivals = nullptr;  // per-unit chunk arrival counters, 0 between steps
+    // Per unit, zero between steps: the decode-step kernel's chunk arrival
+    // counters [units], the scoring kernel's [units], its 64-bit argmin
+    // words [units] (4 words per unit in all).
+    uint32_t* arrivals = nullptr;
     size_t arrivals_len = 0;
 };
 
@@ -66,9 +69,9 @@ lf_status get_scratch(int dev, cudaStream_t stream, size_t need, size_t units, S
             s.arrivals = nullptr;
             s.arrivals_len = 0;
         }
-        cudaError_t e = cudaMalloc(&s.arrivals, units * sizeof(uint32_t));
+        cudaError_t e = cudaMalloc(&s.arrivals, 4 * units * sizeof(uint32_t));
         if (e != cudaSuccess) return fail(LF_ERR_NO_MEMORY, "cudaMalloc(arrival counters): %s", cudaGetErrorString(e));
-        e = cudaMemset(s.arrivals, 0, units * sizeof(uint32_t));
+        e = cudaMemset(s.arrivals, 0, 4 * units * sizeof(uint32_t));
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
         s.arrivals_len = units;
     }
@@ -201,7 +204,11 @@ uint64_t wait_limit_ns() {
 struct Plan {
     int tiles, chunk_tiles, nchunk, stages;
     bool cluster;  // the unit's chunks run as one thread-block cluster
+    bool split;    // a top-1 step scores in a second kernel (split finish)
 };
+
+// Units of at least this many slots take the split finish.
+constexpr int kSplitMinSlots = 8192;
 
 // Split the slot axis of every unit into nchunk chunks of chunk_tiles tiles.
 // Each CTA costs a fixed start-up and merge, so chunks stay long (13 to 32
@@ -250,6 +257,13 @@ Plan plan_split(int S, int units, int sms, bool want_cluster) {
         }
         pl.cluster = true;
     }
+    // Top-1 steps over long units without clusters score in a second kernel:
+    // the last CTA's scan of every slot would otherwise run on the step's
+    // tail at one SM's share of the memory system. LF_SPLIT=0 / 1 forces it
+    // off / on (on: for every top-1 step without clusters).
+    const char* senv = std::getenv("LF_SPLIT");
+    const int smode = senv ? std::atoi(senv) : -1;
+    pl.split = want_cluster && !pl.cluster && smode != 0 && (smode == 1 || S >= kSplitMinSlots);
     return pl;
 }
 
@@ -318,7 +332,7 @@ lf_status check_args(const StepArgs& a, const Shape& s) {
 }
 
 struct Layout {
-    size_t ml, o, stash, total;
+    size_t ml, o, stash, cfold, total;
 };
 
 Layout scratch_layout(const Shape& s, const Plan& pl, size_t extra) {
@@ -328,7 +342,8 @@ Layout scratch_layout(const Shape& s, const Plan& pl, size_t extra) {
     L.ml = 0;
     L.o = align_up(L.ml + units * pl.nchunk * g * sizeof(float2), 256);
     L.stash = align_up(L.o + units * pl.nchunk * g * s.d * sizeof(float), 256);
-    L.total = align_up(L.stash + units * static_cast<size_t>(s.S) * g * sizeof(float), 256) + extra;
+    L.cfold = align_up(L.stash + units * static_cast<size_t>(s.S) * g * sizeof(float), 256);
+    L.total = align_up(L.cfold + units * g * sizeof(float), 256) + extra;
     return L;
 }
 
@@ -359,6 +374,9 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
     sp.stash = reinterpret_cast<float*>(base + L.stash);
     sp.arrivals = scr->arrivals;
     sp.dev_err = scr->dev_err;
+    sp.cfold = reinterpret_cast<float*>(base + L.cfold);
+    sp.score_arrivals = scr->arrivals + units;
+    sp.best = reinterpret_cast<unsigned long long*>(scr->arrivals + 2 * static_cast<size_t>(units));
     sp.Hq = s.Hq;
     sp.Hkv = s.Hkv;
     sp.S = s.S;
@@ -369,29 +387,38 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
     sp.wait_limit_ns = wait_limit_ns();
     sp.topk = a.score ? a.topk : 1;
     sp.flags = a.score ? a.flags : 0;
+    sp.split = (a.score && pl.split && sp.topk == 1) ? 1 : 0;
     if (!lf::step_fits(s.d, g, pl.stages, a.score, pl.nchunk, sp.topk))
         return fail(LF_ERR_UNSUPPORTED,
                     "k = %d with %d chunks of the slot axis does not fit in shared memory",
                     sp.topk, pl.nchunk);
 
+    // A named range around each launch for timeline profilers (nsys).
+    struct NvtxRange {
+        explicit NvtxRange(const char* n) { nvtxRangePushA(n); }
+        ~NvtxRange() { nvtxRangePop(); }
+    };
     cudaError_t e;
     {
-        // A named range around each launch for timeline profilers (nsys).
-        struct NvtxRange {
-            explicit NvtxRange(const char* n) { nvtxRangePushA(n); }
-            ~NvtxRange() { nvtxRangePop(); }
-        } range(a.score ? "lf_decode_step" : "lf_decode_attention");
+        NvtxRange range(a.score ? "lf_decode_step" : "lf_decode_attention");
         ProfScope prof(a.score ? LF_KERNEL_DECODE_STEP : LF_KERNEL_ATTENTION, stream);
         const bool cluster = pl.cluster && sp.topk == 1;
         e = lf::launch_decode_step(s.d, g, pl.stages, a.score, cluster, tmK, tmV, sp, units, stream);
         if (e != cudaSuccess && cluster) {
-            // A cluster that cannot be scheduled: the last-CTA merge instead.
+            // A cluster that cannot be scheduled: the last-CTA merge, scoring
+            // in the same kernel.
             (void)cudaGetLastError();
             e = lf::launch_decode_step(s.d, g, pl.stages, a.score, false, tmK, tmV, sp, units,
                                        stream);
         }
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");
+    if (sp.split) {
+        NvtxRange range("lf_score");
+        ProfScope prof(LF_KERNEL_SCORE, stream);
+        e = lf::launch_score(g, sp, units, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "scoring-kernel launch");
+    }
     return LF_OK;
 }
 

@@ -39,7 +39,10 @@
 // k-at-once compression of the Fig. 3 caption. Empty slots can rank first
 // (cache-fill phase) and the chosen slots can be masked in place.
 // Long units stream their score terms through shared memory with bulk copies
-// for that scan. When the whole grid fits in one wave, a unit's chunks run as
+// for that scan, or, for top-1 steps over units of thousands of slots, leave
+// the scan to a second kernel (the split finish, lf_score_kernel) that scores
+// every chunk of every unit in parallel once the step's memory traffic is
+// over. When the whole grid fits in one wave, a unit's chunks run as
 // one thread-block cluster instead (kCluster): they merge through distributed
 // shared memory and each CTA scores its own chunk (top-1 only).
 // An attention-only instantiation (kScore = false) drops the row norms, the
@@ -49,6 +52,8 @@
 // one before its first global read.
 #include <math.h>
 #include <stdlib.h>
+
+#include <algorithm>
 
 #include "../../include/lf_decode.h"
 #include "lf_kernels.h"
@@ -356,9 +361,15 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int usabl
         const int e = tid + k * kConsumers;
         if (e < G * D) out[e] = __float2bfloat16_rn(o[k]);
     }
-    if constexpr (kScore)
-        score_and_select<G>(p, u, s_m, s_il, red_v, red_j, s_ncand, s_live, topk_area, scan_area,
-                            scan_bytes, scan_bars, tid);
+    if constexpr (kScore) {
+        if (p.split) {
+            // The scoring kernel that follows scores the chunks in parallel.
+            if (tid < G) p.cfold[static_cast<size_t>(u) * G + tid] = __log2f(s_il[tid]) - s_m[tid];
+        } else {
+            score_and_select<G>(p, u, s_m, s_il, red_v, red_j, s_ncand, s_live, topk_area,
+                                scan_area, scan_bytes, scan_bars, tid);
+        }
+    }
     consumer_bar_sync();
     // Every read of the unit's scratch is done: drop the lines, no write-back.
     discard_range(po, static_cast<size_t>(nchunk) * G * D * sizeof(float), tid, kConsumers);
@@ -1244,6 +1255,153 @@ cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepP
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------ split finish --
+//
+// For long units the last CTA's scan of every slot sits on the step's tail,
+// and while the other SMs stream K and V it gets about one SM's share of the
+// memory system. With a split finish the decode-step kernel stops after the
+// merge (publishing c_h per unit) and this kernel, launched behind it with
+// programmatic dependent launch, scores every chunk of every unit in
+// parallel: I_j = sum_h 2^(t_hj + c_h), the same arithmetic in the same order
+// as the single-kernel scan, so scores and choices are bit-identical. The
+// lexicographic (I_j, j) argmin is an atomic maximum over the complemented
+// 64-bit key (score bits + 1, slot), empty slots (fill-empty-first) taking
+// score key 0; the last CTA of the unit reads and clears it.
+constexpr int kScoreThreads = 128;
+constexpr int kScoreWarps = kScoreThreads / 32;
+constexpr int kScoreTilesPerWarp = 2;  // tiles a warp loads per round trip (4 slots per lane)
+constexpr int kScoreMaxChunks = 1024;
+
+// CTA (part, u) scores the chunks [part * per, (part + 1) * per) of unit u,
+// per = ceil(nchunk / parts); the host sizes `parts` so that the whole grid
+// is resident at once. Warps take whole 64-slot tiles, so a tile's chunk and
+// liveness are warp-uniform and a tile of a chunk without a live slot costs
+// no load.
+template <int G>
+__global__ void __launch_bounds__(kScoreThreads, G >= 8 ? 4 : 8) lf_score_kernel(const StepParams p, int parts) {
+    allow_dependent_launch();
+    grid_dependency_wait();
+    __shared__ unsigned char s_live[kScoreMaxChunks];
+    __shared__ unsigned long long s_red[kScoreWarps];
+    const int part = blockIdx.x;
+    const int u = blockIdx.y;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int S = p.S;
+    const int nchunk = p.nchunk;
+    const int ct = p.chunk_tiles;
+    const int per = (nchunk + parts - 1) / parts;
+    const int c0 = part * per;
+    const int c1 = min(nchunk, c0 + per);
+    float* scores = p.scores ? p.scores + static_cast<size_t>(u) * S : nullptr;
+    const bool fill_first = (p.flags & kFlagFillEmptyFirst) != 0;
+    const bool all = fill_first || scores != nullptr;
+    const float* stash = p.stash + static_cast<size_t>(u) * S * G;
+    const int32_t* age = p.mask + static_cast<size_t>(u) * S;
+    // A chunk whose softmax maximum is -inf holds no live slot: no scored
+    // candidate there (empty slots and scores are still visited when wanted).
+    for (int c = c0 + tid; c < c1; c += kScoreThreads)
+        s_live[c - c0] = all || __ldcg(&p.part_ml[(static_cast<size_t>(u) * nchunk + c) * G].x) != -INFINITY;
+    float cf[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) cf[h] = __ldcg(&p.cfold[static_cast<size_t>(u) * G + h]);
+    __syncthreads();
+
+    // Each lane keeps its best (score key, slot). A lane visits its slots in
+    // increasing order, so a strict "<" on the key alone keeps the lowest slot
+    // among equal keys. Key: score bits + 1 (I >= 0, so the bits order like
+    // the values), 0 for an empty slot under fill-empty-first, ~0u for none.
+    uint32_t bkey = 0xffffffffu;
+    int bj = 0x7fffffff;
+    const int tlo = c0 * ct;
+    const int thi = min((S + kTile - 1) / kTile, c1 * ct);
+    // tile / ct by a multiply-high: exact for ct <= 32 and any tile of an int S
+    // (the rounding error of the reciprocal stays below tile / 2^32 < 1 / ct).
+    const uint32_t ct_inv = ct > 1 ? static_cast<uint32_t>((0x100000000ull + ct - 1) / ct) : 0u;
+    const int W = p.W;
+    constexpr int kSlots = 2 * kScoreTilesPerWarp;  // per lane and round trip
+    for (int tb = tlo + warp * kScoreTilesPerWarp; tb < thi;
+         tb += kScoreWarps * kScoreTilesPerWarp) {
+        int a[kSlots];
+        float t[kSlots][G];
+        bool in[kScoreTilesPerWarp];
+#pragma unroll
+        for (int q = 0; q < kScoreTilesPerWarp; ++q) {
+            const int tile = tb + q;
+            const int c = ct > 1 ? static_cast<int>(__umulhi(static_cast<uint32_t>(tile), ct_inv)) : tile;
+            in[q] = tile < thi && s_live[c - c0];  // warp-uniform
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int j = tile * kTile + r * 32 + lane;
+                const bool ok = in[q] && j < S;
+                a[2 * q + r] = ok ? __ldcg(age + j) : -1;
+                if (ok) load_terms<G>(stash + j * G, t[2 * q + r]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kScoreTilesPerWarp; ++q) {
+            if (!in[q]) continue;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int j = (tb + q) * kTile + r * 32 + lane;
+                const int aa = a[2 * q + r];
+                float I = 0.f;
+#pragma unroll
+                for (int h = 0; h < G; ++h) I += ex2_approx(t[2 * q + r][h] + cf[h]);
+                const bool live = aa >= 0;
+                const bool cand = live ? (aa >= W && I == I) : fill_first;
+                const uint32_t key = live ? __float_as_uint(I) + 1u : 0u;
+                if (cand && j < S && key < bkey) {
+                    bkey = key;
+                    bj = j;
+                }
+                if (scores && j < S) scores[j] = live ? I : INFINITY;
+            }
+        }
+    }
+    // (key, slot) minimum of the CTA, as the complemented 64-bit word.
+    unsigned long long best = bkey == 0xffffffffu
+                                  ? 0ull
+                                  : ~((static_cast<unsigned long long>(bkey) << 32) |
+                                      static_cast<uint32_t>(bj));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+        best = o > best ? o : best;
+    }
+    if (lane == 0) s_red[warp] = best;
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+        for (int w = 1; w < kScoreWarps; ++w) best = s_red[w] > best ? s_red[w] : best;
+        bool last = true;
+        if (parts > 1) {
+            if (best) atomicMax(&p.best[u], best);
+            __threadfence();
+            last = atomicAdd(&p.score_arrivals[u], 1u) == static_cast<uint32_t>(parts - 1);
+            if (last) {
+                p.score_arrivals[u] = 0u;
+                __threadfence();
+                best = atomicExch(&p.best[u], 0ull);
+            }
+        }
+        if (last) {
+            const int slot = best ? static_cast<int>(static_cast<uint32_t>(~best)) : -1;
+            p.next_slot[u] = slot;
+            if (slot >= 0 && (p.flags & kFlagMaskEvicted))
+                p.mask[static_cast<size_t>(u) * S + slot] = -1;
+        }
+    }
+    // Every read of these chunks' score terms is done: drop the lines.
+    const int cs = ct * kTile;
+    for (int c = c0; c < c1; ++c)
+        if (s_live[c - c0])
+            discard_range(stash + static_cast<size_t>(c) * cs * G,
+                          static_cast<size_t>(min(S, (c + 1) * cs) - c * cs) * G * 4, tid,
+                          kScoreThreads);
+}
+
 template <int D, int G>
 cudaError_t launch_dg(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
                       int units, cudaStream_t stream, int stages, bool score, bool cluster,
@@ -1254,6 +1412,40 @@ cudaError_t launch_dg(const CUtensorMap& tmK, const CUtensorMap& tmV, const Step
     if (!score) return launch_t<D, G, 2, false, false>(tmK, tmV, p, units, stream, pdl);
     return stages == 2 ? launch_t<D, G, 2, true, false>(tmK, tmV, p, units, stream, pdl)
                        : launch_t<D, G, 3, true, false>(tmK, tmV, p, units, stream, pdl);
+}
+
+template <int G>
+cudaError_t launch_score_t(const StepParams& p, int units, cudaStream_t stream, bool pdl) {
+    // Parts per unit: as many as keep the whole grid resident at once.
+    static int occ[2] = {-1, -1};  // {device, CTAs per SM}
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (occ[0] != dev) {
+        int n = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, lf_score_kernel<G>, kScoreThreads, 0);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        occ[0] = dev;
+        occ[1] = std::max(1, n) * std::max(1, sms);
+    }
+    int parts = occ[1] / std::max(1, units);
+    if (const char* env = std::getenv("LF_SCORE_PARTS")) parts = std::atoi(env);  // tests, tuning
+    parts = std::max(1, std::min(p.nchunk, parts));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(parts, units);
+    cfg.blockDim = dim3(kScoreThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, lf_score_kernel<G>, p, parts);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -1287,6 +1479,19 @@ cudaError_t launch_decode_step(int D, int G, int stages, bool score, bool cluste
     LF_STEP_CASE(128, 1) LF_STEP_CASE(128, 2) LF_STEP_CASE(128, 4) LF_STEP_CASE(128, 8)
 #undef LF_STEP_CASE
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_score(int G, const StepParams& p, int units, cudaStream_t stream) {
+    if (p.chunk_tiles > kMaxChunkTiles || p.nchunk > kScoreMaxChunks) return cudaErrorInvalidValue;
+    const char* env = std::getenv("LF_PDL");
+    const bool pdl = !(env && std::atoi(env) == 0);
+    switch (G) {
+        case 1: return launch_score_t<1>(p, units, stream, pdl);
+        case 2: return launch_score_t<2>(p, units, stream, pdl);
+        case 4: return launch_score_t<4>(p, units, stream, pdl);
+        case 8: return launch_score_t<8>(p, units, stream, pdl);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace lf

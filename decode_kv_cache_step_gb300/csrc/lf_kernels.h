@@ -15,7 +15,8 @@ constexpr int kBoxCols = 64;        // bf16 columns per 128-byte swizzled TMA bo
 // One decode step. Grid (nchunk, units): CTA (c, u) performs the slot write
 // and mask ageing for chunk c of unit u, attends over the chunk's live tiles
 // and leaves softmax partials and per-slot score terms in scratch. The last
-// CTA of a unit to finish merges them: output row, LongFlowScore, argmin.
+// CTA of a unit to finish merges them: output row, LongFlowScore, argmin
+// (with split set, the scoring kernel does the last two).
 struct StepParams {
     const __nv_bfloat16* q;      // [B][Hq][D]
     __nv_bfloat16* k_cache;      // [units][S][D] (row write_slot is written)
@@ -33,6 +34,12 @@ struct StepParams {
     float* stash;                // [units][S][G]          log2(exp(s) * ||v||_1) per live slot
     uint32_t* arrivals;          // [units] chunk arrival counters, 0 between steps
     uint32_t* dev_err;           // LF_DEVERR_* bits
+    // Split finish (top-1 only): the last CTA publishes c_h = log2(1/l_h) - m_h
+    // and a second kernel scores the unit's chunks in parallel.
+    float* cfold = nullptr;                // [units][G]
+    unsigned long long* best = nullptr;    // [units] ~(score key, slot) maximum, 0 between steps
+    uint32_t* score_arrivals = nullptr;    // [units] arrival counters of the scoring kernel
+    int split = 0;
     int Hq, Hkv, S, W, nchunk, chunk_tiles;
     float scale_log2;            // scale * log2(e)
     int topk;                    // slots returned per unit (1 = the argmin)
@@ -62,5 +69,10 @@ bool step_fits(int D, int G, int stages, bool score, int nchunk, int topk);
 cudaError_t launch_decode_step(int D, int G, int stages, bool score, bool cluster,
                                const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const StepParams& p, int units, cudaStream_t stream);
+
+// The scoring kernel of a split finish: grid (nchunk, units); CTA (c, u)
+// scores chunk c of unit u from the ages, the score terms and c_h, and the
+// unit's last CTA writes next_slot (and masks it with kFlagMaskEvicted).
+cudaError_t launch_score(int G, const StepParams& p, int units, cudaStream_t stream);
 
 }  // namespace lf

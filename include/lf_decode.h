@@ -50,6 +50,18 @@
  *
  * Supported shapes: d in {64, 128}; g in {1, 2, 4, 8}; 1 <= S <= 2^20;
  * B * Hkv <= 65535. Anything else returns LF_ERR_UNSUPPORTED.
+ *
+ * Environment switches, read at every call (tuning and tests; every setting
+ * stays within the same tolerances of the exact result, and LF_SPLIT,
+ * LF_SCORE_PARTS and LF_PDL change no result bit):
+ *   LF_CHUNK_TILES=n   64-slot tiles per chunk of the slot axis (1..32)
+ *   LF_STAGES=3        three-stage TMA ring (two CTAs per SM) instead of two
+ *   LF_CLUSTER=0|1     thread-block-cluster merge off / on wherever it fits
+ *   LF_PDL=0           programmatic dependent launch off
+ *   LF_SPLIT=0|1       split finish off / on for every top-1 step without
+ *                      clusters (default: units of at least 8192 slots)
+ *   LF_SCORE_PARTS=n   scoring-kernel CTAs per unit in a split finish
+ *   LF_WAIT_LIMIT_NS=n limit of the pipeline waits (diagnostic)
  */
 #ifndef LF_DECODE_H
 #define LF_DECODE_H
@@ -73,10 +85,17 @@ typedef enum lf_status {
 #define LF_DEVERR_BAD_WRITE_SLOT 0x1u /* a write_slot outside [-1, S) was ignored */
 #define LF_DEVERR_WAIT_TIMEOUT 0x2u   /* a pipeline wait gave up; that step's results are invalid */
 
-/* Kernel ids for lf_profile_collect. A decode step is one launch of one kernel. */
-#define LF_KERNEL_DECODE_STEP 0 /* slot write, mask ageing, attention, score, eviction */
+/*
+ * Kernel ids for lf_profile_collect. A decode step is one launch of the
+ * decode-step kernel, followed, for top-1 steps over long units (a "split
+ * finish"), by one launch of the scoring kernel: the decode-step kernel then
+ * stops after the merge and the scoring kernel computes LongFlowScore and the
+ * argmin of every chunk in parallel.
+ */
+#define LF_KERNEL_DECODE_STEP 0 /* slot write, mask ageing, attention (+ score, eviction) */
 #define LF_KERNEL_ATTENTION 1   /* lf_decode_attention: slot write and attention only */
-#define LF_KERNEL_COUNT 2
+#define LF_KERNEL_SCORE 2       /* split finish: LongFlowScore and eviction */
+#define LF_KERNEL_COUNT 3
 
 /* Flags of lf_decode_step_ex. */
 #define LF_STEP_FILL_EMPTY_FIRST 0x1 /* return empty (masked) slots, lowest first, before any score */

@@ -2,7 +2,7 @@
 graph (with its programmatic-dependent-launch edges) does exactly what the
 eager calls do, and a step is deterministic: the same resident state and
 inputs give the same bits, whichever launch path is taken (PDL on or off,
-cluster merge or last-CTA merge), so a snapshot of (caches, mask, slot) can be
+cluster merge, last-CTA merge or split finish), so a snapshot of (caches, mask, slot) can be
 replayed."""
 import numpy as np
 import pytest
@@ -27,11 +27,14 @@ def _two_steps(wl, state, inputs, stream, ws0, nxt1, nxt2, out):
                        out, nx, wl.W, wl.scale, stream=stream)
 
 
-@pytest.mark.parametrize("name", ["qwen3_8b_b1_s2400", "llama8b_b256_s2400_ragged"])
+@pytest.mark.parametrize("name", ["qwen3_8b_b1_s2400", "llama8b_b256_s2400_ragged",
+                                  "long_b32_s16384_ragged"])
 def test_cuda_graph_replay_equals_eager(name):
+    """The 16K-slot workload takes the split finish: two kernels per step,
+    both chained by programmatic dependent launch inside the graph."""
     wl = WORKLOADS[name]
     if wl.B > 16:
-        wl = wl.with_batch(16)
+        wl = wl.with_batch(16 if wl.S <= 4096 else 2)
     st = initial_state(wl)
     inputs = [{k: to_dev(v) for k, v in step_inputs(wl, t).items()} for t in range(2)]
     shape = (wl.B, wl.Hkv)
@@ -71,7 +74,8 @@ def test_cuda_graph_replay_equals_eager(name):
 
 
 @pytest.mark.parametrize("env", [{}, {"LF_PDL": "0"}, {"LF_CLUSTER": "0"}, {"LF_CLUSTER": "1"},
-                                 {"LF_STAGES": "3"}])
+                                 {"LF_STAGES": "3"}, {"LF_CLUSTER": "0", "LF_SPLIT": "1"},
+                                 {"LF_CLUSTER": "0", "LF_SPLIT": "1", "LF_PDL": "0"}])
 def test_step_is_bitwise_deterministic(monkeypatch, env):
     for k, v in env.items():
         monkeypatch.setenv(k, v)

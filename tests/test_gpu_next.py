@@ -141,10 +141,11 @@ def test_topk_matches_oracle(k):
     check_ex(case, 16, 0.088, k, 0, f"k={k}")
 
 
-@pytest.mark.parametrize("cluster", ["1", "0"])
+@pytest.mark.parametrize("cluster,split", [("1", "0"), ("0", "0"), ("0", "1")])
 @pytest.mark.parametrize("k,flags", [(1, 1), (8, 1), (1, 2), (32, 2), (64, 3), (1, 3)])
-def test_fill_first_and_mask_evicted(monkeypatch, k, flags, cluster):
+def test_fill_first_and_mask_evicted(monkeypatch, k, flags, cluster, split):
     monkeypatch.setenv("LF_CLUSTER", cluster)
+    monkeypatch.setenv("LF_SPLIT", split)
     rng = np.random.default_rng(600 + 10 * k + flags)
     case = _pins.rand_case(rng, 3, 4, 2, 64, 700, p_masked=0.05, max_age=3000)
     check_ex(case, 8, 0.125, k, flags, f"k={k} flags={flags}")

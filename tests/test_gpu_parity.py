@@ -129,21 +129,26 @@ def test_host_io_entry_point_matches_device_entry_point():
     assert torch.equal(a.mask, b.mask) and torch.equal(a.k, b.k)
 
 
-@pytest.mark.parametrize("cluster", ["1", "0"])
+@pytest.mark.parametrize("cluster,split", [("1", "0"), ("0", "0"), ("0", "1")])
 @pytest.mark.parametrize("chunk_tiles", ["1", "3", "32"])
-def test_split_shapes_do_not_change_results(monkeypatch, chunk_tiles, cluster):
+def test_split_shapes_do_not_change_results(monkeypatch, chunk_tiles, cluster, split):
     """Different slot-axis splits, merged inside a thread-block cluster or by
-    the unit's last CTA, give results within tolerance of the oracle."""
+    the unit's last CTA (scoring there or in the split-finish kernel), give
+    results within tolerance of the oracle."""
     monkeypatch.setenv("LF_CHUNK_TILES", chunk_tiles)
     monkeypatch.setenv("LF_CLUSTER", cluster)
+    monkeypatch.setenv("LF_SPLIT", split)
     wl = WORKLOADS["long_b32_s16384_ragged"].with_batch(2)
     run_parity(wl, steps=2)
 
 
+@pytest.mark.parametrize("split", ["0", "1"])
 @pytest.mark.parametrize("name", ["qwen3_8b_b1_s2400", "tiny_b2_s256"])
-def test_last_cta_merge_path_every_step(monkeypatch, name):
+def test_last_cta_merge_path_every_step(monkeypatch, name, split):
     """The merge by the unit's last CTA (used when clusters are off or a unit
-    has more than 8 chunks) on every step of the small workloads."""
+    has more than 8 chunks) on every step of the small workloads, scoring in
+    the same kernel or in the split-finish kernel."""
     monkeypatch.setenv("LF_CLUSTER", "0")
+    monkeypatch.setenv("LF_SPLIT", split)
     wl = WORKLOADS[name]
     run_parity(wl, min(wl.steps, 32))

@@ -144,7 +144,7 @@ __device__ __forceinline__ void discard_range(const void* p, size_t bytes, int t
         discard_l2_line(reinterpret_cast<const void*>(line));
 }
 
-// Lexicographic (key, slot) order for the top-k list.
+// Lexicographic (key, slot) order of selection candidates.
 __device__ __forceinline__ bool key_less(uint32_t ka, int ja, uint32_t kb, int jb) {
     return ka < kb || (ka == kb && ja < jb);
 }
@@ -439,35 +439,32 @@ __device__ void score_and_select(const StepParams& p, int u, const float* s_m, c
     // Chunks without a live slot hold no scored candidate; they are visited
     // only when empty slots are candidates or every score is wanted.
     const bool all = fill_first || scores != nullptr;
-    float best = INFINITY;
+    const int W = p.W;
+    // Selection key of a candidate: the score's bits + 1 (I >= 0 orders like
+    // its bits), 0 for an empty slot under fill-empty-first; ~0u: none.
+    uint32_t bkey = 0xffffffffu;  // top-1: this thread's best (key, slot)
     int bestj = 0x7fffffff;
     int ncand = 0;
 
     auto visit = [&](int j, int a, const float* t) {
-        float I = INFINITY;
-        bool cand = false;
-        float cval = 0.f;
-        if (a >= 0) {
-            I = 0.f;
+        float I = 0.f;
 #pragma unroll
-            for (int h = 0; h < G; ++h) I += ex2_approx(t[h] + c[h]);
-            cand = a >= p.W && !isnan(I);
-            cval = I;
-        } else if (fill_first) {
-            cand = true;
-            cval = -1.f;
-        }
+        for (int h = 0; h < G; ++h) I += ex2_approx(t[h] + c[h]);
+        const bool live = a >= 0;
+        const bool cand = live ? (a >= W && I == I) : fill_first;
+        const uint32_t key = live ? __float_as_uint(I) + 1u : 0u;
         if (top1) {
-            if (cand && better(cval, j, best, bestj)) {
-                best = cval;
+            // A thread visits its slots in increasing order, so a strict "<"
+            // keeps the lowest slot among equal keys.
+            if (cand && key < bkey) {
+                bkey = key;
                 bestj = j;
             }
         } else {
-            keys[static_cast<size_t>(j) * G] =
-                !cand ? 0xffffffffu : (cval < 0.f ? 0u : __float_as_uint(cval) + 1u);
+            keys[static_cast<size_t>(j) * G] = cand ? key : 0xffffffffu;
             ncand += cand ? 1 : 0;
         }
-        if (scores) scores[j] = I;
+        if (scores) scores[j] = live ? I : INFINITY;
     };
 
     if (!all && !top1) {
@@ -588,25 +585,26 @@ __device__ void score_and_select(const StepParams& p, int u, const float* s_m, c
     if (top1) {
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, best, off);
+            const uint32_t ok = __shfl_xor_sync(0xffffffffu, bkey, off);
             const int oj = __shfl_xor_sync(0xffffffffu, bestj, off);
-            if (better(ov, oj, best, bestj)) {
-                best = ov;
+            if (key_less(ok, oj, bkey, bestj)) {
+                bkey = ok;
                 bestj = oj;
             }
         }
+        uint32_t* red_k = reinterpret_cast<uint32_t*>(red_v);
         if ((tid & 31) == 0) {
-            red_v[tid >> 5] = best;
+            red_k[tid >> 5] = bkey;
             red_j[tid >> 5] = bestj;
         }
         consumer_bar_sync();
         if (tid == 0) {
             for (int w = 1; w < kConsumerWarps; ++w)
-                if (better(red_v[w], red_j[w], best, bestj)) {
-                    best = red_v[w];
+                if (key_less(red_k[w], red_j[w], bkey, bestj)) {
+                    bkey = red_k[w];
                     bestj = red_j[w];
                 }
-            const int slot = (bestj == 0x7fffffff) ? -1 : bestj;
+            const int slot = (bkey == 0xffffffffu) ? -1 : bestj;
             p.next_slot[u] = slot;
             if (slot >= 0 && (p.flags & kFlagMaskEvicted))
                 p.mask[static_cast<size_t>(u) * S + slot] = -1;

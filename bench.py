@@ -514,8 +514,10 @@ def bench_lf(args, wl):
         "cpu_baseline": cpu,
         "e2e": {"value": world * args.steps / e2e_s, "unit": "steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "lf_decode_step_host per layer from pinned host buffers; "
-                       "stream sync every step"},
+                "how": "lf_decode_step_host per layer from pinned host buffers (the kernel "
+                       "reads inputs and writes results in host memory in place over the "
+                       "host link; LF_HOST_ZEROCOPY=0 stages them with copies); stream sync "
+                       "every step"},
         "gpu_launches": args.steps * L * launches_per_layer,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }

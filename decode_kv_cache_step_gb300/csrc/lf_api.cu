@@ -173,7 +173,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // [units][S][D] bf16 as a 3-D tensor map, 64 x 64 x 1 boxes, 128-byte swizzle.
-lf_status encode_cache_map(CUtensorMap* m, void* base, int D, int S, int units) {
+lf_status encode_cache_map_uncached(CUtensorMap* m, void* base, int D, int S, int units) {
     auto enc = tensor_map_encoder();
     if (!enc) return fail(LF_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
@@ -186,6 +186,41 @@ lf_status encode_cache_map(CUtensorMap* m, void* base, int D, int S, int units) 
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(LF_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
+    return LF_OK;
+}
+
+// A tensor map is a pure function of (base, D, S, units), so the maps of the
+// caches a caller steps over are kept (a small round-robin table) instead of
+// being encoded again at every call.
+struct MapKey {
+    void* base;
+    int D, S, units;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && D == o.D && S == o.S && units == o.units;
+    }
+};
+constexpr int kMapCacheSize = 64;
+std::mutex g_map_mu;
+MapKey g_map_keys[kMapCacheSize] = {};
+CUtensorMap g_maps[kMapCacheSize];
+int g_map_next = 0;
+
+lf_status encode_cache_map(CUtensorMap* m, void* base, int D, int S, int units) {
+    const MapKey k{base, D, S, units};
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        for (int i = 0; i < kMapCacheSize; ++i)
+            if (g_map_keys[i].base && g_map_keys[i] == k) {
+                *m = g_maps[i];
+                return LF_OK;
+            }
+    }
+    lf_status st = encode_cache_map_uncached(m, base, D, S, units);
+    if (st != LF_OK) return st;
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    g_map_keys[g_map_next] = k;
+    g_maps[g_map_next] = *m;
+    g_map_next = (g_map_next + 1) % kMapCacheSize;
     return LF_OK;
 }
 
@@ -538,18 +573,43 @@ lf_status lf_decode_step_host(const void* q_host, void* k_cache, void* v_cache, 
     Scratch* scr = nullptr;
     if ((st = get_scratch(dev, stream, L.total, static_cast<size_t>(s.B) * s.Hkv, &scr)) != LF_OK) return st;
     char* stg = static_cast<char*>(scr->base) + (L.total - staging);
-    StepArgs a{stg + off_q, k_cache, v_cache, mask, stg + off_k, stg + off_v,
-               reinterpret_cast<int32_t*>(stg + off_w), stg + off_o,
-               reinterpret_cast<int32_t*>(stg + off_n), nullptr};
+    // Page-locked host buffers that this device can address (cudaHostAlloc /
+    // cudaHostRegister memory; on GB300 over NVLink-C2C) are read and written
+    // by the kernel in place; any other buffer goes through device staging
+    // with one copy each way. LF_HOST_ZEROCOPY=0 stages every buffer.
+    const char* zenv = std::getenv("LF_HOST_ZEROCOPY");
+    const bool zero_copy = !(zenv && std::atoi(zenv) == 0);
+    auto mapped = [&](const void* p, size_t align) -> void* {
+        if (!zero_copy) return nullptr;
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        if (at.type != cudaMemoryTypeHost || !at.devicePointer ||
+            reinterpret_cast<uintptr_t>(at.devicePointer) % align != 0)
+            return nullptr;
+        return at.devicePointer;
+    };
+    void* dq = mapped(q_host, 16);
+    void* dk = mapped(new_k_host, 16);
+    void* dv = mapped(new_v_host, 16);
+    void* dw = mapped(write_slot_host, 4);
+    void* dout = mapped(out_host, 16);
+    void* dn = mapped(next_slot_host, 4);
+    StepArgs a{dq ? dq : stg + off_q, k_cache, v_cache, mask, dk ? dk : stg + off_k,
+               dv ? dv : stg + off_v,
+               reinterpret_cast<int32_t*>(dw ? dw : stg + off_w), dout ? dout : stg + off_o,
+               reinterpret_cast<int32_t*>(dn ? dn : stg + off_n), nullptr};
     g_last_error[0] = '\0';
-    if ((e = cudaMemcpyAsync(stg + off_q, q_host, q_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(stg + off_k, new_k_host, kv_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(stg + off_v, new_v_host, kv_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(stg + off_w, write_slot_host, i_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+    if ((!dq && (e = cudaMemcpyAsync(stg + off_q, q_host, q_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess) ||
+        (!dk && (e = cudaMemcpyAsync(stg + off_k, new_k_host, kv_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess) ||
+        (!dv && (e = cudaMemcpyAsync(stg + off_v, new_v_host, kv_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess) ||
+        (!dw && (e = cudaMemcpyAsync(stg + off_w, write_slot_host, i_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess))
         return cuda_fail(e, "host-to-device copy");
     if ((st = enqueue_step(a, s, stream, scr, L, pl)) != LF_OK) return st;
-    if ((e = cudaMemcpyAsync(out_host, stg + off_o, q_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(next_slot_host, stg + off_n, i_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+    if ((!dout && (e = cudaMemcpyAsync(out_host, stg + off_o, q_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess) ||
+        (!dn && (e = cudaMemcpyAsync(next_slot_host, stg + off_n, i_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess))
         return cuda_fail(e, "device-to-host copy");
     return LF_OK;
 }

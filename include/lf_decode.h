@@ -62,6 +62,7 @@
  *                      clusters (default: units of at least 8192 slots)
  *   LF_SCORE_PARTS=n   scoring-kernel CTAs per unit in a split finish
  *   LF_WAIT_LIMIT_NS=n limit of the pipeline waits (diagnostic)
+ *   LF_HOST_ZEROCOPY=0 lf_decode_step_host stages every host buffer
  */
 #ifndef LF_DECODE_H
 #define LF_DECODE_H
@@ -175,12 +176,20 @@ lf_status lf_decode_attention(const void* q, void* k_cache, void* v_cache, int32
 
 /*
  * One decode step whose per-step inputs and outputs live in HOST memory, for
- * callers that drive decoding from the CPU. q, new_k, new_v and write_slot are
- * copied host -> device, the step runs, and out and next_slot are copied
- * device -> host, all enqueued on `stream` (pinned host buffers make the copies
- * asynchronous). The caches and the mask stay on the device (device pointers),
- * as they are the decoder's resident state. The host output buffers are valid
- * after the stream synchronises. Staging lives in the library's scratch.
+ * callers that drive decoding from the CPU. The caches and the mask stay on
+ * the device (device pointers), as they are the decoder's resident state.
+ * Each host buffer (q, new_k, new_v, write_slot in; out, next_slot out) is
+ * used one of two ways, chosen per buffer at every call:
+ *   - page-locked memory that the current device can address (cudaHostAlloc
+ *     or cudaHostRegister; reported by cudaPointerGetAttributes with a device
+ *     pointer) and aligned like the device arrays (16 bytes for bf16, 4 for
+ *     int32) is read or written by the kernel in place, with no copy (on
+ *     GB300 over NVLink-C2C);
+ *   - any other buffer is copied through device staging in the library's
+ *     scratch (host -> device before the step, device -> host after it, on
+ *     `stream`). LF_HOST_ZEROCOPY=0 stages every buffer.
+ * The host inputs must not change, and the outputs must not be read, until
+ * the stream has synchronised.
  */
 lf_status lf_decode_step_host(const void* q_host, void* k_cache, void* v_cache, int32_t* mask,
                               const void* new_k_host, const void* new_v_host,

@@ -109,7 +109,13 @@ def test_scoreless_entry_point_matches_scores_variant():
     assert torch.equal(a.mask, b.mask) and torch.equal(a.k, b.k) and torch.equal(a.v, b.v)
 
 
-def test_host_io_entry_point_matches_device_entry_point():
+@pytest.mark.parametrize("io", ["pinned", "pageable", "mixed", "pinned_staged"])
+def test_host_io_entry_point_matches_device_entry_point(monkeypatch, io):
+    """lf_decode_step_host: pinned buffers are used in place by the kernel,
+    pageable ones go through device staging (mixed: some of each); both give
+    the device entry point's bits."""
+    if io == "pinned_staged":
+        monkeypatch.setenv("LF_HOST_ZEROCOPY", "0")
     wl = WORKLOADS["llama8b_b256_s2400_ragged"].with_batch(8)
     st = initial_state(wl)
     inp = step_inputs(wl, 2)
@@ -117,11 +123,18 @@ def test_host_io_entry_point_matches_device_entry_point():
     a = DevState(st["k_cache"], st["v_cache"], st["mask"], wl.Hq)
     b = DevState(st["k_cache"], st["v_cache"], st["mask"], wl.Hq)
     ra = a.step(inp["q"], inp["new_k"], inp["new_v"], ws, wl.W, wl.scale, scores=False)
-    pin = lambda x: torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x).pin_memory()
-    q, nk, nv, w = pin(inp["q"]), pin(inp["new_k"]), pin(inp["new_v"]), pin(ws)
+    def host(x, pinned):
+        t = torch.from_numpy((x.view(np.int16) if x.dtype == np.uint16 else x).copy())
+        return t.pin_memory() if pinned else t
+    pins = {"pinned": [True] * 6, "pinned_staged": [True] * 6, "pageable": [False] * 6,
+            "mixed": [True, False, True, False, False, True]}[io]
+    q, nk, nv, w = (host(inp["q"], pins[0]), host(inp["new_k"], pins[1]),
+                    host(inp["new_v"], pins[2]), host(ws, pins[3]))
     q, nk, nv = q.view(torch.bfloat16), nk.view(torch.bfloat16), nv.view(torch.bfloat16)
-    out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.bfloat16).pin_memory()
-    nxt = torch.empty((wl.B, wl.Hkv), dtype=torch.int32).pin_memory()
+    out = torch.full((wl.B, wl.Hq, wl.d), 7.0, dtype=torch.bfloat16)
+    nxt = torch.full((wl.B, wl.Hkv), -5, dtype=torch.int32)
+    out = out.pin_memory() if pins[4] else out
+    nxt = nxt.pin_memory() if pins[5] else nxt
     lf.decode_step_host(q, b.k, b.v, b.mask, nk, nv, w, out, nxt, wl.W, wl.scale)
     torch.cuda.synchronize()
     assert np.array_equal(out.float().numpy().astype(np.float64), ra["out"])

@@ -281,7 +281,7 @@ def bench_lf(args, wl):
     layers = [(k, v, mask)] + [(k.clone(), v.clone(), mask.clone()) for _ in range(L - 1)]
     slots = [[torch.full((wl.B, wl.Hkv), -1, dtype=torch.int32, device=device),
               torch.empty((wl.B, wl.Hkv), dtype=torch.int32, device=device)] for _ in range(L)]
-    use_graph = L > 1
+    use_graph = L > 1 and not args.eager
     stream = torch.cuda.Stream(device) if use_graph else torch.cuda.current_stream(device)
 
     def step_eager(i, layer_ids=None):
@@ -545,6 +545,9 @@ def main():
     ap.add_argument("--layers", type=int, default=1,
                     help="decode through L layers' caches per step (one CUDA graph per "
                          "token when L > 1); Qwen3-8B has 36")
+    ap.add_argument("--eager", action="store_true",
+                    help="with --layers > 1: launch the layers' steps one by one instead "
+                         "of replaying a CUDA graph")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps, always
     wl = WORKLOADS[args.workload]

@@ -125,6 +125,10 @@ def _stream_handle(stream) -> int | None:
 
 
 def _need(t: torch.Tensor, name: str, dtype, shape, cuda: bool):
+    # One combined test on the common path; the detailed ones name the fault.
+    if (isinstance(t, torch.Tensor) and t.dtype is dtype and t.shape == shape
+            and t.is_cuda is cuda and t.is_contiguous()):
+        return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name}: expected a torch.Tensor")
     if t.dtype != dtype:

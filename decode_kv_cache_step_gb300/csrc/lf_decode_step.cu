@@ -894,8 +894,11 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
     // Slot write, part 1 (Fig. 2 Left): age the chunk's mask. The written slot
     // gets age 0 (and becomes live); other live slots age by one. Every load
     // is issued before any store, so the chunk's mask costs one round trip.
+    // The aged entries are stored evict-last: the next step reads them again,
+    // and between the two the K/V stream passes through L2 evict-first.
     constexpr int kPer = (kMaxChunkTiles * kTile + kThreads - 1) / kThreads;
     int32_t* mrow = p.mask + static_cast<size_t>(u) * S + slot0;
+    const uint64_t mask_pol = l2_policy_evict_last();
     int av[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
@@ -913,7 +916,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
                     na = (slot0 + i == ws) ? 0 : ((a >= 0 && a != 0x7fffffff) ? a + 1 : a);
                 else
                     na = (slot0 + i == ws && a < 0) ? 0 : a;  // the written slot is live
-                if (na != a) mrow[i] = na;
+                if (na != a) st_global_hint(mrow + i, na, mask_pol);
                 a = na;
             }
             ages[i] = a;

@@ -162,22 +162,46 @@ def bf16_dev(a, device):
     return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
 
 
-def run_oracle_steps(wl, state, max_seconds: float, max_steps: int, units=None):
-    """Times oracle steps (the CPU baseline); returns (steps, seconds, threads)."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
+def run_oracle_steps(wl, state, max_seconds: float, max_steps: int, units=None, nthreads=0):
+    """Times oracle steps (the CPU baseline); returns (steps, seconds, threads,
+    per-step seconds). nthreads = 0 uses every OpenMP thread."""
     import oracle
     ws = np.full((wl.B, wl.Hkv), -1, dtype=np.int32)
-    done, t_total = 0, 0.0
+    done, t_total, times = 0, 0.0, []
     while done < max_steps and (t_total < max_seconds or done == 0):
         inp = step_inputs(wl, 1000 + done)
         t0 = time.perf_counter()
         res = oracle.decode_step(inp["q"], state["k_cache"], state["v_cache"], state["mask"],
-                                 inp["new_k"], inp["new_v"], ws, wl.W, wl.scale, units=units)
-        t_total += time.perf_counter() - t0
+                                 inp["new_k"], inp["new_v"], ws, wl.W, wl.scale, units=units,
+                                 nthreads=nthreads)
+        times.append(time.perf_counter() - t0)
+        t_total += times[-1]
         ws = res["next_slot"].copy()
         if units is not None:
             ws[ws < -1] = -1
         done += 1
-    return done, t_total, oracle.max_threads()
+    return done, t_total, (nthreads if nthreads > 0 else oracle.max_threads()), times
 
 
 def bench_reference(args, wl):
@@ -463,10 +487,12 @@ def bench_lf(args, wl):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        n, secs, threads = run_oracle_steps(wl, host, max_seconds=args.cpu_seconds, max_steps=50)
+        n, secs, threads, times = run_oracle_steps(wl, host, max_seconds=args.cpu_seconds,
+                                                   max_steps=50, nthreads=args.cpu_threads)
         cpu = {"value": n / secs / L, "unit": "steps/s", "cores": threads, "kind": "oracle",
                "sample": f"{n} full decode step(s) of one layer of the same workload, fp64, "
-                         f"{threads} OpenMP threads" + (f", divided by {L} layers" if L > 1 else "")}
+                         f"{threads} OpenMP threads" + (f", divided by {L} layers" if L > 1 else ""),
+               "median_step_s": float(np.median(times)), "cpu_model": cpu_model()}
 
     if rank != 0:
         return 0
@@ -540,6 +566,8 @@ def main():
     ap.add_argument("--reference-units", type=int, default=64,
                     help="(b,kvh) units the reference arm runs per step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="OpenMP threads of the CPU baseline (0: all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overhead", action="store_true",
                     help="skip the attention-only comparison")

@@ -44,7 +44,8 @@ METRIC = "decode steps/s and achieved HBM GB/s (% of GB300 peak) for fused attn+
 DEFAULT_WORKLOAD = "qwen3_8b_b128_s3200"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "lf_decode_step_kernel.qwen3_8b_b128_s3200.md")
-KERNEL_SOURCES = ["lf_decode_step.cu", "lf_ptx.cuh", "lf_kernels.h"]
+KERNEL_SOURCES = ["lf_step_kernel.cuh", "lf_decode_step.cu", "lf_decode_step_cluster.cu",
+                  "lf_ptx.cuh", "lf_kernels.h"]
 
 
 def kernel_source_hash() -> str:

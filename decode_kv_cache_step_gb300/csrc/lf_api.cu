@@ -291,6 +291,17 @@ Plan plan_split(int S, int units, int sms, bool want_cluster) {
             pl.nchunk = (pl.tiles + pl.chunk_tiles - 1) / pl.chunk_tiles;
         }
         pl.cluster = true;
+        // A grid of at most one CTA per SM has room for a deep TMA ring: every
+        // tile of a short chunk is in flight at once, which shortens the
+        // chain of round trips of a latency-bound step. It pays from 5 tiles
+        // per chunk (3 turns of a 2-stage ring; measured: one 2400-slot
+        // sequence 12.5 -> 11.5 us per step, a 4-tile chunk no gain).
+        // LF_DEEP=0: off; LF_DEEP=1: also for shorter chunks.
+        const char* denv = std::getenv("LF_DEEP");
+        const int dmode = denv ? std::atoi(denv) : -1;
+        if (dmode != 0 && static_cast<long>(units) * pl.nchunk <= static_cast<long>(sms) &&
+            (dmode == 1 || pl.chunk_tiles >= 5))
+            pl.stages = lf::kDeepStages;
     }
     // Top-1 steps over long units without clusters score in a second kernel:
     // the last CTA's scan of every slot would otherwise run on the step's
@@ -443,8 +454,7 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
             // A cluster that cannot be scheduled: the last-CTA merge, scoring
             // in the same kernel.
             (void)cudaGetLastError();
-            e = lf::launch_decode_step(s.d, g, pl.stages, a.score, false, tmK, tmV, sp, units,
-                                       stream);
+            e = lf::launch_decode_step(s.d, g, 2, a.score, false, tmK, tmV, sp, units, stream);
         }
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");

@@ -1,1260 +1,11 @@
-// The LongFlow decode-step kernel (sm_103a): slot write, split-KV attention,
-// LongFlowScore and eviction in one launch.
-//
-// "LongFlow: Efficient KV Cache Compression for Reasoning Models":
-//   Fig. 2 (Left)   the current K/V covers the slot chosen at the previous step,
-//                   then the static KV and Mask go to the kernel with Q, which
-//                   returns the output and the slot to cover next;
-//   Fig. 2 (Middle) K, V and the Mask stream from HBM into on-chip memory by
-//                   block and the attention runs there;
-//   Fig. 2 (Right)  P.V is split in two: G = p * v (per slot) and O = sum_j G.
-//                   LongFlowScore is read off G. With the score
-//                   I_j = sum_h sum_c |p_hj v_jc| = (sum_h p_hj) * ||v_j||_1
-//                   (p >= 0), G never has to exist: each live slot leaves
-//                   t_hj = log2(exp(s_hj) * ||v_j||_1) per head, and the final
-//                   I_j = sum_h 2^(t_hj - m_h) / l_h once m_h, l_h are known;
-//   Fig. 1 caption  one token is evicted after every attention call.
-//
-// Grid (nchunk, units). CTA (c, u) owns chunk c (up to 32 tiles of 64 slots)
-// of unit u = (b, kvh):
-//   warp 4, lane 0 : producer. TMA-loads the K and V tiles of the chunk's
-//                    live tiles (128-byte swizzled boxes, 2- or 3-stage
-//                    mbarrier ring, L2 evict-first: each byte is read once
-//                    per step).
-//   warps 0..3     : consumers. Warp w owns rows 16w..16w+15 of every tile
-//                    and keeps its own online-softmax state. Per 16 slots:
-//        S^T[16 x 8]  = K[16 x D] . Q^T[D x 8]       (mma m16n8k16, heads as N)
-//        N  [16 x 8]  = |V|[16 x D] . 1[D x 8]        (row L1 norms on the MMA)
-//        O^T[D x 8]  += V^T[D x 16] . P^T[16 x 8]     (P^T via movmatrix)
-//   GQA folding: the g <= 8 query heads of the unit share each K/V byte.
-//   Masked slots are removed by select (logit -inf, V columns zeroed), so
-//   NaN or Inf in masked rows never reaches the output.
-// The CTA then publishes its chunk's (m, l, O) and counts itself in. The last
-// CTA of the unit merges the chunks, writes the output row, finishes
-// LongFlowScore for every live slot, selects the slots to evict and drops the
-// unit's scratch lines from L2 without writing them back. The selection is
-// the lexicographic (I_j, j) argmin over slots with age >= W, or, for k > 1,
-// the k smallest by an 8-bit radix select on the score bits (then on the slot
-// index among equal scores) and a bitonic sort of the k winners; the periodic
-// k-at-once compression of the Fig. 3 caption. Empty slots can rank first
-// (cache-fill phase) and the chosen slots can be masked in place.
-// Long units stream their score terms through shared memory with bulk copies
-// for that scan, or, for top-1 steps over units of thousands of slots, leave
-// the scan to a second kernel (the split finish, lf_score_kernel) that scores
-// every chunk of every unit in parallel once the step's memory traffic is
-// over. When the whole grid fits in one wave, a unit's chunks run as
-// one thread-block cluster instead (kCluster): they merge through distributed
-// shared memory and each CTA scores its own chunk (top-1 only).
-// An attention-only instantiation (kScore = false) drops the row norms, the
-// score terms, the ageing and the selection: the baseline for the overhead.
-// Launches use programmatic dependent launch: a CTA lets the next kernel of
-// the stream start launching as soon as it starts, and waits for the previous
-// one before its first global read.
-#include <math.h>
-#include <stdlib.h>
-
-#include <algorithm>
-
-#include "../../include/lf_decode.h"
-#include "lf_kernels.h"
-#include "lf_ptx.cuh"
+// Instantiations of the decode-step kernel that merge in the unit's last CTA
+// (2- and 3-stage TMA rings, score on or off), the split-finish scoring
+// kernel, and the launch dispatch; the thread-block-cluster instantiations
+// live in lf_decode_step_cluster.cu so that the two compile in parallel.
+#include "lf_step_kernel.cuh"
 
 namespace lf {
 namespace {
-
-constexpr int kConsumerWarps = 4;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
-constexpr uint32_t kOnesBf16x2 = 0x3F803F80u;   // (1.0, 1.0) in bf16
-constexpr uint32_t kAbsBf16x2 = 0x7FFF7FFFu;
-
-template <int D, int kStages>
-struct StepSmem {
-    static constexpr int kBoxes = D / kBoxCols;
-    static constexpr int kBoxBytes = kTile * 128;              // 64 rows x 128 B
-    static constexpr int kTensorBytes = kBoxes * kBoxBytes;    // K (or V) of one tile
-    static constexpr int kStageBytes = 2 * kTensorBytes;       // K + V
-    static constexpr int kAgesOff = kStages * kStageBytes;
-    static constexpr int kAgesBytes = kMaxChunkTiles * kTile * 4;
-    static constexpr int kListOff = kAgesOff + kAgesBytes;
-    static constexpr int kMiscOff = kListOff + kMaxChunkTiles * 4;
-    static constexpr int kBarOff = kMiscOff + 16;
-    static constexpr int kScanBarOff = kBarOff + 2 * kStages * 8;  // the finish's 2 barriers
-    static constexpr int kBytes = kScanBarOff + 16;
-    static constexpr int kAlloc = kBytes + 1024;               // slack for 1024-B alignment
-};
-
-__device__ __forceinline__ void consumer_bar_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-}
-
-// Consumer barrier that also returns whether any consumer passed `pred`.
-__device__ __forceinline__ bool consumer_bar_or(bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, 1, %2, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "n"(kConsumers)
-        : "memory");
-    return r != 0;
-}
-
-// Byte offset of 16-byte chunk `cg` (8 bf16 columns) of tile row `row` in a
-// swizzled K or V tile buffer.
-constexpr int kBoxBytes = kTile * 128;  // one 64-row x 128-byte swizzled box
-
-__device__ __forceinline__ uint32_t swz_off(int row, int cg) {
-    return (cg >> 3) * kBoxBytes + row * 128 + (((cg & 7) ^ (row & 7)) << 4);
-}
-
-__device__ __forceinline__ bool better(float v, int j, float bv, int bj) {
-    return v < bv || (v == bv && j < bj);
-}
-
-template <int G>
-__device__ __forceinline__ void load_terms(const float* t, float (&v)[G]) {
-    if constexpr (G == 1) {
-        v[0] = __ldcg(t);
-    } else if constexpr (G == 2) {
-        const float2 a = __ldcg(reinterpret_cast<const float2*>(t));
-        v[0] = a.x;
-        v[1] = a.y;
-    } else {
-#pragma unroll
-        for (int q = 0; q < G / 4; ++q) {
-            const float4 a = __ldcg(reinterpret_cast<const float4*>(t) + q);
-            v[4 * q] = a.x;
-            v[4 * q + 1] = a.y;
-            v[4 * q + 2] = a.z;
-            v[4 * q + 3] = a.w;
-        }
-    }
-}
-
-// Drops the 128-byte lines lying wholly inside [p, p + bytes).
-__device__ __forceinline__ void discard_range(const void* p, size_t bytes, int tid, int nthreads) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uintptr_t first = (a + 127) & ~static_cast<uintptr_t>(127);
-    const uintptr_t end = (a + bytes) & ~static_cast<uintptr_t>(127);
-    for (uintptr_t line = first + static_cast<uintptr_t>(tid) * 128; line < end;
-         line += static_cast<uintptr_t>(nthreads) * 128)
-        discard_l2_line(reinterpret_cast<const void*>(line));
-}
-
-// Lexicographic (key, slot) order of selection candidates.
-__device__ __forceinline__ bool key_less(uint32_t ka, int ja, uint32_t kb, int jb) {
-    return ka < kb || (ka == kb && ja < jb);
-}
-
-// One 8-bit radix-select pass over the unit's candidate keys: among values v
-// with (v & pmask) == prefix, finds the digit (v >> shift) & 255 holding the
-// `remaining`-th smallest and returns the rank left inside that digit. With
-// by_slot the value is the slot index of keys equal to `tie_key`.
-__device__ __forceinline__ int radix_pass(const uint32_t* keys, int stride, int S, int shift,
-                                          uint32_t pmask, uint32_t prefix, int remaining,
-                                          bool by_slot, uint32_t tie_key, int* hist,
-                                          int* s_out, int tid, uint32_t* digit_out) {
-    for (int i = tid; i < 256; i += kConsumers) hist[i] = 0;
-    consumer_bar_sync();
-    for (int j = tid; j < S; j += kConsumers) {
-        const uint32_t key = __ldcg(keys + static_cast<size_t>(j) * stride);
-        if (key == 0xffffffffu) continue;
-        const uint32_t v = by_slot ? static_cast<uint32_t>(j) : key;
-        if (by_slot && key != tie_key) continue;
-        if ((v & pmask) == prefix) atomicAdd(&hist[(v >> shift) & 255], 1);
-    }
-    consumer_bar_sync();
-    if (tid == 0) {
-        int cum = 0, d = 255;
-        for (int b = 0; b < 256; ++b) {
-            if (cum + hist[b] >= remaining) {
-                d = b;
-                break;
-            }
-            cum += hist[b];
-        }
-        s_out[0] = d;
-        s_out[1] = remaining - cum;
-    }
-    consumer_bar_sync();
-    *digit_out = static_cast<uint32_t>(s_out[0]);
-    return s_out[1];
-}
-
-// Shared memory of select_topk: histogram, scalars, the winners' keys and slots.
-constexpr int kTopKAreaBytes = (256 + 4) * 4 + 2 * kMaxTopK * 4;
-
-// The k smallest (key, slot) pairs of a unit, ascending, into next_slot[u][k]
-// (-1 past the number of candidates). Keys were written one per slot (stride
-// `stride` words); 0xffffffff marks a slot that is not a candidate.
-__device__ void select_topk(const StepParams& p, int u, const uint32_t* keys, int stride,
-                            int ncand, uint8_t* area, int tid) {
-    const int S = p.S;
-    const int k = p.topk;
-    int* hist = reinterpret_cast<int*>(area);              // [256]
-    int* s_out = hist + 256;                               // [4]
-    uint32_t* l_key = reinterpret_cast<uint32_t*>(s_out + 4);  // [kMaxTopK]
-    int* l_idx = reinterpret_cast<int*>(l_key + kMaxTopK);     // [kMaxTopK]
-    const int keff = min(k, ncand);
-    int32_t* out = p.next_slot + static_cast<size_t>(u) * k;
-    if (keff > 0) {
-        // Threshold key T: the keff-th smallest key.
-        uint32_t prefix = 0, pmask = 0;
-        int remaining = keff;
-        for (int pass = 0; pass < 4; ++pass) {
-            const int shift = 24 - 8 * pass;
-            uint32_t dgt;
-            remaining = radix_pass(keys, stride, S, shift, pmask, prefix, remaining, false, 0u,
-                                   hist, s_out, tid, &dgt);
-            prefix |= dgt << shift;
-            pmask |= 0xffu << shift;
-        }
-        const uint32_t T = prefix;
-        // Among keys equal to T, the `remaining` lowest slots: slot threshold J.
-        uint32_t iprefix = 0, ipmask = 0;
-        for (int pass = 0; pass < 3; ++pass) {
-            const int shift = 16 - 8 * pass;
-            uint32_t dgt;
-            remaining = radix_pass(keys, stride, S, shift, ipmask, iprefix, remaining, true, T,
-                                   hist, s_out, tid, &dgt);
-            iprefix |= dgt << shift;
-            ipmask |= 0xffu << shift;
-        }
-        const int J = static_cast<int>(iprefix);
-        if (tid == 0) s_out[2] = 0;
-        consumer_bar_sync();
-        for (int j = tid; j < S; j += kConsumers) {
-            const uint32_t key = __ldcg(keys + static_cast<size_t>(j) * stride);
-            if (key == 0xffffffffu) continue;
-            if (key < T || (key == T && j <= J)) {
-                const int pos = atomicAdd(&s_out[2], 1);
-                if (pos < kMaxTopK) {
-                    l_key[pos] = key;
-                    l_idx[pos] = j;
-                }
-            }
-        }
-        consumer_bar_sync();
-        // Bitonic sort of the keff winners by (key, slot).
-        int n2 = 1;
-        while (n2 < keff) n2 <<= 1;
-        for (int i = keff + tid; i < n2; i += kConsumers) {
-            l_key[i] = 0xffffffffu;
-            l_idx[i] = 0x7fffffff;
-        }
-        consumer_bar_sync();
-        for (int size = 2; size <= n2; size <<= 1) {
-            for (int stride2 = size >> 1; stride2 > 0; stride2 >>= 1) {
-                for (int i = tid; i < n2; i += kConsumers) {
-                    const int ixj = i ^ stride2;
-                    if (ixj > i) {
-                        const bool up = (i & size) == 0;
-                        const bool swap = up ? key_less(l_key[ixj], l_idx[ixj], l_key[i], l_idx[i])
-                                             : key_less(l_key[i], l_idx[i], l_key[ixj], l_idx[ixj]);
-                        if (swap) {
-                            const uint32_t tk = l_key[i];
-                            const int ti = l_idx[i];
-                            l_key[i] = l_key[ixj];
-                            l_idx[i] = l_idx[ixj];
-                            l_key[ixj] = tk;
-                            l_idx[ixj] = ti;
-                        }
-                    }
-                }
-                consumer_bar_sync();
-            }
-        }
-    }
-    for (int i = tid; i < k; i += kConsumers) {
-        const int slot = (i < keff) ? l_idx[i] : -1;
-        out[i] = slot;
-        if (slot >= 0 && (p.flags & kFlagMaskEvicted))
-            p.mask[static_cast<size_t>(u) * S + slot] = -1;
-    }
-}
-
-template <int G>
-__device__ void score_and_select(const StepParams& p, int u, const float* s_m, const float* s_il,
-                                 float* red_v, int* red_j, int* s_ncand, const int* s_live,
-                                 uint8_t* topk_area, uint8_t* scan_area, int scan_bytes,
-                                 uint64_t* scan_bars, int tid);
-
-// Merge of the unit's chunks by its last CTA (consumer threads only). The
-// shared memory below `usable` is free; scan_bars are two spare mbarriers.
-template <int D, int G, bool kScore>
-__device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int usable,
-                            uint64_t* scan_bars, int tid) {
-    const int nchunk = p.nchunk;
-    float* s_w = reinterpret_cast<float*>(smem);  // [nchunk][G]: 2^(m_c - m) / l
-    float* s_m = s_w + nchunk * G;                // [G]
-    float* s_il = s_m + G;                        // [G]
-    float* red_v = s_il + G;                      // [4]
-    int* red_j = reinterpret_cast<int*>(red_v + kConsumerWarps);
-    int* s_ncand = red_j + kConsumerWarps;
-    int* s_live = s_ncand + 4;                    // [nchunk]: 1 if the chunk has a live slot
-    uint8_t* topk_area = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(s_live + nchunk) + 15) & ~static_cast<uintptr_t>(15));
-    uint8_t* scan_area = topk_area + (p.topk > 1 ? kTopKAreaBytes : 0);
-    const int scan_bytes = usable - static_cast<int>(scan_area - smem);
-    const float2* ml = p.part_ml + static_cast<size_t>(u) * nchunk * G;
-
-    if (tid < G) {
-        float m = -INFINITY;
-        for (int c = 0; c < nchunk; ++c) m = fmaxf(m, __ldcg(&ml[c * G + tid]).x);
-        float l = 0.f;
-        for (int c = 0; c < nchunk; ++c) {
-            const float2 v = __ldcg(&ml[c * G + tid]);
-            if (v.x != -INFINITY) l += v.y * exp2f(v.x - m);
-        }
-        s_m[tid] = m;
-        s_il[tid] = (l > 0.f) ? 1.f / l : 0.f;
-    }
-    if (tid == 0) s_ncand[0] = 0;
-    consumer_bar_sync();
-    for (int e = tid; e < nchunk * G; e += kConsumers) {
-        const float2 v = __ldcg(&ml[e]);
-        const int h = e % G;
-        s_w[e] = (v.x == -INFINITY) ? 0.f : exp2f(v.x - s_m[h]) * s_il[h];
-        if (h == 0) s_live[e / G] = v.x != -INFINITY;  // m = -inf: no live slot
-    }
-    consumer_bar_sync();
-
-    // Output: O_h = sum_c w_ch * O_ch, rounded to bf16.
-    const int b = u / p.Hkv;
-    const int kvh = u - b * p.Hkv;
-    const float* po = p.part_o + static_cast<size_t>(u) * nchunk * G * D;
-    __nv_bfloat16* out = p.out + (static_cast<size_t>(b) * p.Hq + kvh * G) * D;
-    // Loads of four chunks are issued together; a chunk that had no live
-    // tile has weight 0 and its (unwritten) partial is selected away.
-    constexpr int kPerT = (G * D + kConsumers - 1) / kConsumers;
-    float o[kPerT];
-#pragma unroll
-    for (int k = 0; k < kPerT; ++k) o[k] = 0.f;
-    for (int c0 = 0; c0 < nchunk; c0 += 4) {
-        float v[4][kPerT];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const int c = min(c0 + cc, nchunk - 1);
-#pragma unroll
-            for (int k = 0; k < kPerT; ++k) {
-                const int e = tid + k * kConsumers;
-                v[cc][k] = (e < G * D) ? __ldcg(&po[static_cast<size_t>(c) * G * D + e]) : 0.f;
-            }
-        }
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const int c = c0 + cc;
-            if (c >= nchunk) break;
-#pragma unroll
-            for (int k = 0; k < kPerT; ++k) {
-                const int e = tid + k * kConsumers;
-                const float w = (e < G * D) ? s_w[c * G + e / D] : 0.f;
-                o[k] += (w != 0.f) ? w * v[cc][k] : 0.f;
-            }
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < kPerT; ++k) {
-        const int e = tid + k * kConsumers;
-        if (e < G * D) out[e] = __float2bfloat16_rn(o[k]);
-    }
-    if constexpr (kScore) {
-        if (p.split) {
-            // The scoring kernel that follows scores the chunks in parallel.
-            if (tid < G) p.cfold[static_cast<size_t>(u) * G + tid] = __log2f(s_il[tid]) - s_m[tid];
-        } else {
-            score_and_select<G>(p, u, s_m, s_il, red_v, red_j, s_ncand, s_live, topk_area,
-                                scan_area, scan_bytes, scan_bars, tid);
-        }
-    }
-    consumer_bar_sync();
-    // Every read of the unit's scratch is done: drop the lines, no write-back.
-    discard_range(po, static_cast<size_t>(nchunk) * G * D * sizeof(float), tid, kConsumers);
-}
-
-// Segments of a unit's slot axis that the score scan visits, in order: pieces
-// of at most `seg` slots of the runs of consecutive chunks that hold a live
-// slot (of all chunks when `all` is set). The same walk runs in every
-// consumer thread.
-struct SegWalk {
-    int j0;    // first slot of the current segment (>= S: done)
-    int rend;  // end of the current run of chunks
-};
-
-__device__ __forceinline__ int next_chunk(int c, int nchunk, const int* s_live, bool all) {
-    while (c < nchunk && !(all || s_live[c])) ++c;
-    return c;
-}
-
-// Starts a run at chunk c (or ends the walk when c == nchunk).
-__device__ __forceinline__ SegWalk seg_run(int c, int cs, int S, int nchunk, const int* s_live,
-                                           bool all) {
-    if (c >= nchunk) return SegWalk{S, S};
-    int e = c;
-    while (e + 1 < nchunk && (all || s_live[e + 1])) ++e;
-    return SegWalk{c * cs, min((e + 1) * cs, S)};
-}
-
-__device__ __forceinline__ int seg_end(const SegWalk& w, int seg) { return min(w.j0 + seg, w.rend); }
-
-__device__ __forceinline__ void seg_advance(SegWalk& w, int cs, int seg, int S, int nchunk,
-                                            const int* s_live, bool all) {
-    const int e = seg_end(w, seg);
-    if (e < w.rend)
-        w.j0 = e;
-    else
-        w = seg_run(next_chunk((w.rend + cs - 1) / cs, nchunk, s_live, all), cs, S, nchunk,
-                    s_live, all);
-}
-
-// Units with more slots to score than this stream them through shared memory.
-constexpr int kBulkScanMinSlots = 4096;
-
-// LongFlowScore of every live slot of unit u and the selection of the slots to
-// evict, by the unit's last CTA once the final (m_h, l_h) are known.
-template <int G>
-__device__ void score_and_select(const StepParams& p, int u, const float* s_m, const float* s_il,
-                                 float* red_v, int* red_j, int* s_ncand, const int* s_live,
-                                 uint8_t* topk_area, uint8_t* scan_area, int scan_bytes,
-                                 uint64_t* scan_bars, int tid) {
-    // Candidates: live slots with age >= W and, with kFlagFillEmptyFirst,
-    // empty slots (ranked before every score, lowest slot first).
-    // I_j = sum_h 2^(t_hj - m_h) / l_h = sum_h 2^(t_hj + c_h), c_h = log2(1/l_h) - m_h.
-    float c[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) c[h] = __log2f(s_il[h]) - s_m[h];
-    const int S = p.S;
-    const int nchunk = p.nchunk;
-    const int cs = p.chunk_tiles * kTile;
-    const int32_t* age = p.mask + static_cast<size_t>(u) * S;
-    float* stash = p.stash + static_cast<size_t>(u) * S * G;
-    // For top-k the slot's first stash word is reused for its selection key.
-    uint32_t* keys = reinterpret_cast<uint32_t*>(stash);
-    float* scores = p.scores ? p.scores + static_cast<size_t>(u) * S : nullptr;
-    const bool fill_first = (p.flags & kFlagFillEmptyFirst) != 0;
-    const bool top1 = p.topk == 1;
-    // Chunks without a live slot hold no scored candidate; they are visited
-    // only when empty slots are candidates or every score is wanted.
-    const bool all = fill_first || scores != nullptr;
-    const int W = p.W;
-    // Selection key of a candidate: the score's bits + 1 (I >= 0 orders like
-    // its bits), 0 for an empty slot under fill-empty-first; ~0u: none.
-    uint32_t bkey = 0xffffffffu;  // top-1: this thread's best (key, slot)
-    int bestj = 0x7fffffff;
-    int ncand = 0;
-
-    auto visit = [&](int j, int a, const float* t) {
-        float I = 0.f;
-#pragma unroll
-        for (int h = 0; h < G; ++h) I += ex2_approx(t[h] + c[h]);
-        const bool live = a >= 0;
-        const bool cand = live ? (a >= W && I == I) : fill_first;
-        const uint32_t key = live ? __float_as_uint(I) + 1u : 0u;
-        if (top1) {
-            // A thread visits its slots in increasing order, so a strict "<"
-            // keeps the lowest slot among equal keys.
-            if (cand && key < bkey) {
-                bkey = key;
-                bestj = j;
-            }
-        } else {
-            keys[static_cast<size_t>(j) * G] = cand ? key : 0xffffffffu;
-            ncand += cand ? 1 : 0;
-        }
-        if (scores) scores[j] = live ? I : INFINITY;
-    };
-
-    if (!all && !top1) {
-        // Top-k reads a key for every slot: skipped chunks hold no candidate.
-        for (int c = 0; c < nchunk; ++c)
-            if (!s_live[c])
-                for (int j = c * cs + tid; j < min(S, (c + 1) * cs); j += kConsumers)
-                    keys[static_cast<size_t>(j) * G] = 0xffffffffu;
-    }
-
-    // A long scan streams each segment's ages and score terms into shared memory
-    // with bulk copies, two segments in flight, so it runs at L2 bandwidth
-    // instead of one round trip per slot.
-    constexpr int kSlotBytes = (G + 1) * 4;
-    int seg = (scan_bytes / 2) / kSlotBytes;
-    seg = min(2048, seg & ~(kConsumers - 1));
-    // Short units are cheaper with loads batched in registers (one or two
-    // round trips); long ones stream through shared memory.
-    int nlive = 0;
-    for (int c = 0; c < nchunk; ++c) nlive += (all || s_live[c]) ? 1 : 0;
-    const bool bulk = seg >= kConsumers && nlive * cs > kBulkScanMinSlots && (S & 3) == 0 &&
-                      (reinterpret_cast<uintptr_t>(p.mask) & 15) == 0;
-    if (bulk) {
-        const int half = seg * kSlotBytes;
-        uint8_t* buf0 = reinterpret_cast<uint8_t*>(
-            (reinterpret_cast<uintptr_t>(scan_area) + 15) & ~static_cast<uintptr_t>(15));
-        if (tid == 0) {
-            mbar_init(&scan_bars[0], 1);
-            mbar_init(&scan_bars[1], 1);
-            fence_barrier_init();
-            // The ages and score terms were written through the generic proxy
-            // (here and by the unit's other CTAs); the copies read them through
-            // the async proxy.
-            asm volatile("fence.proxy.async;" ::: "memory");
-        }
-        consumer_bar_sync();
-        SegWalk wi = seg_run(next_chunk(0, nchunk, s_live, all), cs, S, nchunk, s_live, all);
-        SegWalk wc = wi;
-        int issued = 0;
-        auto issue = [&](int s_idx) {
-            const int j1 = seg_end(wi, seg);
-            const int n = j1 - wi.j0;
-            uint8_t* b = buf0 + (s_idx & 1) * half;
-            uint64_t* bar = &scan_bars[s_idx & 1];
-            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * kSlotBytes));
-            bulk_load(b, age + wi.j0, static_cast<uint32_t>(n * 4), bar);
-            bulk_load(b + seg * 4, stash + static_cast<size_t>(wi.j0) * G,
-                      static_cast<uint32_t>(n * G * 4), bar);
-            seg_advance(wi, cs, seg, S, nchunk, s_live, all);
-        };
-        if (tid == 0) {
-            for (; issued < 2 && wi.j0 < S; ++issued) issue(issued);
-        }
-        int s_idx = 0;
-        for (; wc.j0 < S; ++s_idx) {
-            const int b = s_idx & 1;
-            const bool timed_out = !mbar_wait(&scan_bars[b], (s_idx >> 1) & 1, p.wait_limit_ns);
-            if (consumer_bar_or(timed_out)) {
-                if (tid == 0) {
-                    atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
-                    // Copies still in flight land before the CTA retires.
-                    for (int q = s_idx; q < issued; ++q)
-                        (void)mbar_wait(&scan_bars[q & 1], (q >> 1) & 1);
-                }
-                break;
-            }
-            const int32_t* s_age = reinterpret_cast<const int32_t*>(buf0 + b * half);
-            const float* s_t = reinterpret_cast<const float*>(buf0 + b * half + seg * 4);
-            const int n = seg_end(wc, seg) - wc.j0;
-#pragma unroll 4
-            for (int i = tid; i < n; i += kConsumers) {
-                float t[G];
-                if constexpr (G >= 4) {
-#pragma unroll
-                    for (int q4 = 0; q4 < G / 4; ++q4) {
-                        const float4 v = reinterpret_cast<const float4*>(s_t + i * G)[q4];
-                        t[4 * q4] = v.x;
-                        t[4 * q4 + 1] = v.y;
-                        t[4 * q4 + 2] = v.z;
-                        t[4 * q4 + 3] = v.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int h = 0; h < G; ++h) t[h] = s_t[i * G + h];
-                }
-                visit(wc.j0 + i, s_age[i], t);
-            }
-            consumer_bar_sync();  // everyone is done with buffer b
-            if (tid == 0 && wi.j0 < S) issue(issued++);
-            seg_advance(wc, cs, seg, S, nchunk, s_live, all);
-        }
-    } else {
-        // Batches of loads in flight per thread (also for slot counts that
-        // break the 16-byte copy alignment).
-        constexpr int kBatch = 8;
-        for (int j0 = tid; j0 < S; j0 += kBatch * kConsumers) {
-            int a[kBatch];
-            float t[kBatch][G];
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int j = j0 + k * kConsumers;
-                a[k] = (j < S) ? __ldcg(&age[j]) : -1;
-            }
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int j = j0 + k * kConsumers;
-                if (j < S) load_terms<G>(stash + static_cast<size_t>(j) * G, t[k]);
-            }
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int j = j0 + k * kConsumers;
-                if (j >= S) break;
-                visit(j, a[k], t[k]);  // a slot of a chunk with no live slot is no candidate
-            }
-        }
-    }
-
-    if (top1) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const uint32_t ok = __shfl_xor_sync(0xffffffffu, bkey, off);
-            const int oj = __shfl_xor_sync(0xffffffffu, bestj, off);
-            if (key_less(ok, oj, bkey, bestj)) {
-                bkey = ok;
-                bestj = oj;
-            }
-        }
-        uint32_t* red_k = reinterpret_cast<uint32_t*>(red_v);
-        if ((tid & 31) == 0) {
-            red_k[tid >> 5] = bkey;
-            red_j[tid >> 5] = bestj;
-        }
-        consumer_bar_sync();
-        if (tid == 0) {
-            for (int w = 1; w < kConsumerWarps; ++w)
-                if (key_less(red_k[w], red_j[w], bkey, bestj)) {
-                    bkey = red_k[w];
-                    bestj = red_j[w];
-                }
-            const int slot = (bkey == 0xffffffffu) ? -1 : bestj;
-            p.next_slot[u] = slot;
-            if (slot >= 0 && (p.flags & kFlagMaskEvicted))
-                p.mask[static_cast<size_t>(u) * S + slot] = -1;
-        }
-    } else {
-        if (ncand) atomicAdd(s_ncand, ncand);
-        consumer_bar_sync();
-        select_topk(p, u, keys, G, s_ncand[0], topk_area, tid);
-    }
-    consumer_bar_sync();
-    discard_range(stash, static_cast<size_t>(S) * G * sizeof(float), tid, kConsumers);
-}
-
-// Shared-memory bytes finish_unit needs (it reuses the pipeline buffers).
-__host__ __device__ constexpr size_t finish_smem_bytes(int nchunk, int G, int topk) {
-    return (static_cast<size_t>(nchunk) * (G + 1) + 2 * G + 2 * kConsumerWarps + 4) * 4 + 16 +
-           (topk > 1 ? kTopKAreaBytes : 0);
-}
-
-// Epilogue when the unit's chunks run as one thread-block cluster (rank =
-// chunk). The chunk's merged (m, l, O) stay in shared memory; after a
-// cluster barrier every CTA reads its peers' through distributed shared
-// memory. CTA r writes its slice of the output row, every CTA scores only
-// its own chunk's slots, and rank 0 reduces the cluster's (I_j, j) argmin.
-// wO/wm/wl hold the four consumer warps' states (consumer threads only; the
-// producer warp joins the three cluster barriers on its own).
-template <int D, int G, bool kScore>
-__device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
-                                 const int32_t* ages, uint8_t* smem, const float* wO,
-                                 const float* wm, const float* wl, int cnt, int tid) {
-    const int nchunk = p.nchunk;
-    const uint32_t rank = cluster_ctarank();
-    constexpr int kWBytes = (kConsumerWarps * G * D + 2 * kConsumerWarps * G) * 4;
-    float* pub_o = reinterpret_cast<float*>(smem + ((kWBytes + 15) & ~15));  // [G][D]
-    float2* pub_ml = reinterpret_cast<float2*>(pub_o + G * D);               // [G]
-    float* pub_best = reinterpret_cast<float*>(pub_ml + G);                  // [1]
-    int* pub_bestj = reinterpret_cast<int*>(pub_best + 1);                   // [1]
-    float2* s_mlc = reinterpret_cast<float2*>(pub_bestj + 3);                // [nchunk][G]
-    float* s_w = reinterpret_cast<float*>(s_mlc + kMaxClusterChunks * G);    // [nchunk][G]
-    float* s_m = s_w + kMaxClusterChunks * G;                               // [G]
-    float* s_il = s_m + G;                                                   // [G]
-    float* red_v = s_il + G;                                                 // [4]
-    int* red_j = reinterpret_cast<int*>(red_v + kConsumerWarps);             // [4]
-    const float NEG = -INFINITY;
-
-    // This chunk's merged state, published for the cluster.
-    for (int e = tid; e < G * D; e += kConsumers) {
-        const int h = e / D;
-        float mh = NEG;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) mh = fmaxf(mh, wm[w * G + h]);
-        float o = 0.f;
-        if (cnt > 0) {
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float mw = wm[w * G + h];
-                if (mw != NEG) o += wO[w * G * D + e] * exp2f(mw - mh);
-            }
-        }
-        pub_o[e] = o;
-    }
-    if (tid < G) {
-        float mh = NEG, l = 0.f;
-        if (cnt > 0) {
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) mh = fmaxf(mh, wm[w * G + tid]);
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float mw = wm[w * G + tid];
-                if (mw != NEG) l += wl[w * G + tid] * exp2f(mw - mh);
-            }
-        } else {
-            mh = NEG;
-        }
-        pub_ml[tid] = make_float2(mh, l);
-    }
-    cluster_sync();  // #1: every chunk's state is published
-
-    for (int e = tid; e < nchunk * G; e += kConsumers) {
-        const uint32_t a = dsmem_addr(&pub_ml[e % G], static_cast<uint32_t>(e / G));
-        s_mlc[e] = make_float2(ld_dsmem_f32(a), ld_dsmem_f32(a + 4));
-    }
-    consumer_bar_sync();
-    if (tid < G) {
-        float m = NEG;
-        for (int c = 0; c < nchunk; ++c) m = fmaxf(m, s_mlc[c * G + tid].x);
-        float l = 0.f;
-        for (int c = 0; c < nchunk; ++c) {
-            const float2 v = s_mlc[c * G + tid];
-            if (v.x != NEG) l += v.y * exp2f(v.x - m);
-        }
-        s_m[tid] = m;
-        s_il[tid] = (l > 0.f) ? 1.f / l : 0.f;
-    }
-    consumer_bar_sync();
-    for (int e = tid; e < nchunk * G; e += kConsumers) {
-        const float2 v = s_mlc[e];
-        const int h = e % G;
-        s_w[e] = (v.x == NEG) ? 0.f : exp2f(v.x - s_m[h]) * s_il[h];
-    }
-    consumer_bar_sync();
-
-    // This CTA's slice of the output row: O_h = sum_c w_ch * O_ch.
-    {
-        const int b = u / p.Hkv;
-        const int kvh = u - b * p.Hkv;
-        __nv_bfloat16* out = p.out + (static_cast<size_t>(b) * p.Hq + kvh * G) * D;
-        const int per = (G * D + nchunk - 1) / nchunk;
-        const int e0 = static_cast<int>(rank) * per;
-        const int e1 = min(G * D, e0 + per);
-        for (int e = e0 + tid; e < e1; e += kConsumers) {
-            const int h = e / D;
-            float o = 0.f;
-            for (int c = 0; c < nchunk; ++c) {
-                const float w = s_w[c * G + h];
-                const float v = ld_dsmem_f32(dsmem_addr(&pub_o[e], static_cast<uint32_t>(c)));
-                o += (w != 0.f) ? w * v : 0.f;
-            }
-            out[e] = __float2bfloat16_rn(o);
-        }
-    }
-
-    if constexpr (kScore) {
-        // LongFlowScore of this chunk's slots and their local best candidate.
-        float cexp[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) cexp[h] = __log2f(s_il[h]) - s_m[h];
-        const int S = p.S;
-        const float* stash = p.stash + static_cast<size_t>(u) * S * G;
-        float* scores = p.scores ? p.scores + static_cast<size_t>(u) * S : nullptr;
-        const bool fill_first = (p.flags & kFlagFillEmptyFirst) != 0;
-        float best = INFINITY;
-        int bestj = 0x7fffffff;
-        constexpr int kBatch = 8;
-        for (int i0 = tid; i0 < n; i0 += kBatch * kConsumers) {
-            float t[kBatch][G];
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int i = i0 + k * kConsumers;
-                if (i < n && ages[i] >= 0)
-                    load_terms<G>(stash + static_cast<size_t>(slot0 + i) * G, t[k]);
-            }
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int i = i0 + k * kConsumers;
-                if (i >= n) break;
-                const int a = ages[i];
-                const int j = slot0 + i;
-                float I = INFINITY;
-                bool cand = false;
-                float cval = 0.f;
-                if (a >= 0) {
-                    I = 0.f;
-#pragma unroll
-                    for (int h = 0; h < G; ++h) I += ex2_approx(t[k][h] + cexp[h]);
-                    cand = a >= p.W && !isnan(I);
-                    cval = I;
-                } else if (fill_first) {
-                    cand = true;
-                    cval = -1.f;
-                }
-                if (cand && better(cval, j, best, bestj)) {
-                    best = cval;
-                    bestj = j;
-                }
-                if (scores) scores[j] = I;
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, best, off);
-            const int oj = __shfl_xor_sync(0xffffffffu, bestj, off);
-            if (better(ov, oj, best, bestj)) {
-                best = ov;
-                bestj = oj;
-            }
-        }
-        if ((tid & 31) == 0) {
-            red_v[tid >> 5] = best;
-            red_j[tid >> 5] = bestj;
-        }
-        consumer_bar_sync();
-        if (tid == 0) {
-            for (int w = 1; w < kConsumerWarps; ++w)
-                if (better(red_v[w], red_j[w], best, bestj)) {
-                    best = red_v[w];
-                    bestj = red_j[w];
-                }
-            *pub_best = best;
-            *pub_bestj = bestj;
-        }
-        // This chunk's score terms are read: drop them from L2, no write-back.
-        discard_range(stash + static_cast<size_t>(slot0) * G, static_cast<size_t>(n) * G * 4, tid,
-                      kConsumers);
-    }
-    cluster_sync();  // #2: every output slice is written, every local best published
-
-    if (kScore && rank == 0 && tid == 0) {
-        float best = INFINITY;
-        int bestj = 0x7fffffff;
-        for (int c = 0; c < nchunk; ++c) {
-            const float v = ld_dsmem_f32(dsmem_addr(pub_best, static_cast<uint32_t>(c)));
-            const int j = ld_dsmem_s32(dsmem_addr(pub_bestj, static_cast<uint32_t>(c)));
-            if (better(v, j, best, bestj)) {
-                best = v;
-                bestj = j;
-            }
-        }
-        const int slot = (bestj == 0x7fffffff) ? -1 : bestj;
-        p.next_slot[u] = slot;
-        if (slot >= 0 && (p.flags & kFlagMaskEvicted))
-            p.mask[static_cast<size_t>(u) * p.S + slot] = -1;
-    }
-    cluster_sync();  // #3: no CTA leaves while a peer may still read its memory
-}
-
-// kStages-deep TMA ring; 3 stages run 2 CTAs per SM, 2 stages run 3.
-// kScore = false is the attention-only variant (no ageing, score or eviction).
-// kCluster: the grid is launched in clusters of nchunk CTAs (one per unit).
-template <int D, int G, int kStages, bool kScore, bool kCluster>
-__global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : 2)
-    lf_decode_step_kernel(const __grid_constant__ CUtensorMap tmK,
-                          const __grid_constant__ CUtensorMap tmV, const StepParams p) {
-    using L = StepSmem<D, kStages>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    int32_t* ages = reinterpret_cast<int32_t*>(smem + L::kAgesOff);
-    int32_t* list = reinterpret_cast<int32_t*>(smem + L::kListOff);
-    // [0] live tile count, [1] abort flag, [2] last-CTA flag
-    volatile int32_t* misc = reinterpret_cast<int32_t*>(smem + L::kMiscOff);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-    uint64_t* empty = full + kStages;
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    const int chunk = blockIdx.x;
-    const int u = blockIdx.y;
-    const int S = p.S;
-    const int slot0 = chunk * p.chunk_tiles * kTile;
-    const int slot_end = min(slot0 + p.chunk_tiles * kTile, S);
-    const int n = slot_end - slot0;
-    const int ntiles = (n + kTile - 1) / kTile;
-
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
-        }
-        misc[1] = 0;
-        fence_barrier_init();
-    }
-    // With programmatic dependent launch this CTA may start while the previous
-    // kernel of the stream (often the previous decode step) is still running:
-    // everything above touches only this CTA's shared memory; every global
-    // read comes after the wait. The next step may begin launching as soon as
-    // every CTA of this one has started.
-    allow_dependent_launch();
-    grid_dependency_wait();
-
-    int ws = p.write_slot[u];
-    if (ws < -1 || ws >= S) {
-        if (tid == 0 && chunk == 0) atomicOr(p.dev_err, LF_DEVERR_BAD_WRITE_SLOT);
-        ws = -1;
-    }
-
-    // Q^T as the B operand of S^T = K . Q^T, loaded early so its latency
-    // overlaps the mask prologue: b0 = (d = 16kk + h0 .. +1, head r), b1 = d + 8.
-    const int b = u / p.Hkv;
-    const int kvh = u - b * p.Hkv;
-    const int r = lane >> 2;          // fragment row (slot) 0..7
-    const int h0 = 2 * (lane & 3);    // fragment columns (heads) h0, h0+1
-    uint32_t qf[D / 16][2];
-    if (warp < kConsumerWarps) {
-        const bool valid = r < G;
-        const __nv_bfloat16* qrow =
-            p.q + (static_cast<size_t>(b) * p.Hq + kvh * G + (valid ? r : 0)) * D;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const int dc = kk * 16 + h0;
-            qf[kk][0] = valid ? *reinterpret_cast<const uint32_t*>(qrow + dc) : 0u;
-            qf[kk][1] = valid ? *reinterpret_cast<const uint32_t*>(qrow + dc + 8) : 0u;
-        }
-    }
-
-    // Slot write, part 1 (Fig. 2 Left): age the chunk's mask. The written slot
-    // gets age 0 (and becomes live); other live slots age by one. Every load
-    // is issued before any store, so the chunk's mask costs one round trip.
-    // The aged entries are stored evict-last: the next step reads them again,
-    // and between the two the K/V stream passes through L2 evict-first.
-    constexpr int kPer = (kMaxChunkTiles * kTile + kThreads - 1) / kThreads;
-    int32_t* mrow = p.mask + static_cast<size_t>(u) * S + slot0;
-    const uint64_t mask_pol = l2_policy_evict_last();
-    int av[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-        const int i = tid + k * kThreads;
-        av[k] = (i < n) ? mrow[i] : -1;
-    }
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-        const int i = tid + k * kThreads;
-        if (i < n) {
-            int a = av[k];
-            if (ws >= 0) {
-                int na;
-                if constexpr (kScore)
-                    na = (slot0 + i == ws) ? 0 : ((a >= 0 && a != 0x7fffffff) ? a + 1 : a);
-                else
-                    na = (slot0 + i == ws && a < 0) ? 0 : a;  // the written slot is live
-                if (na != a) st_global_hint(mrow + i, na, mask_pol);
-                a = na;
-            }
-            ages[i] = a;
-        }
-    }
-    __threadfence();  // the aged mask is read by the unit's last CTA
-    __syncthreads();
-
-    // Tiles with no live slot are never loaded (ragged fills stream only
-    // their live part).
-    if (warp == 0) {
-        int cnt = 0;
-        for (int t = 0; t < ntiles; ++t) {
-            const int i0 = t * kTile + lane;
-            const int i1 = i0 + 32;
-            const bool live = (i0 < n && ages[i0] >= 0) || (i1 < n && ages[i1] >= 0);
-            if (__any_sync(0xffffffffu, live)) {
-                if (lane == 0) list[cnt] = t;
-                ++cnt;
-            }
-        }
-        if (lane == 0) misc[0] = cnt;
-    }
-    __syncthreads();
-    const int cnt = misc[0];
-
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------ producer --
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            int issued = 0;
-            for (int i = 0; i < cnt; ++i) {
-                const int s = i % kStages;
-                if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, p.wait_limit_ns)) {
-                    atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
-                    misc[1] = 1;
-                    break;
-                }
-                if (misc[1]) break;
-                uint8_t* kb = smem + s * L::kStageBytes;
-                uint8_t* vb = kb + L::kTensorBytes;
-                mbar_arrive_expect_tx(&full[s], L::kStageBytes);
-                const int y = slot0 + list[i] * kTile;
-#pragma unroll
-                for (int bx = 0; bx < L::kBoxes; ++bx) {
-                    tma_load_3d(kb + bx * L::kBoxBytes, &tmK, bx * kBoxCols, y, u, &full[s], pol);
-                    tma_load_3d(vb + bx * L::kBoxBytes, &tmV, bx * kBoxCols, y, u, &full[s], pol);
-                }
-                ++issued;
-            }
-            // Every issued copy has landed before the CTA may retire.
-            for (int i = max(0, issued - kStages); i < issued; ++i)
-                (void)mbar_wait(&full[i % kStages], (i / kStages) & 1);
-        }
-        if constexpr (kCluster) {
-            __syncwarp();
-            cluster_sync();  // the consumers' cluster barriers #1, #2, #3
-            cluster_sync();
-            cluster_sync();
-        }
-        return;
-    }
-
-    // --------------------------------------------------------- consumers --
-    const bool hv0 = h0 < G;
-    const bool hv1 = h0 + 1 < G;
-    const float NEG = -INFINITY;
-
-    float acc[D / 16][4];
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-    float m0 = NEG, m1 = NEG, l0 = 0.f, l1 = 0.f;
-    const float sl = p.scale_log2;
-    const int wrow0 = warp * 16;
-
-    for (int i = 0; i < cnt; ++i) {
-        const int s = i % kStages;
-        if (!mbar_wait(&full[s], (i / kStages) & 1, p.wait_limit_ns)) {
-            if (lane == 0) atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
-            misc[1] = 1;
-            break;
-        }
-        uint8_t* kb = smem + s * L::kStageBytes;
-        uint8_t* vb = kb + L::kTensorBytes;
-        const int tslot0 = slot0 + list[i] * kTile;
-
-        // Slot write, part 2: the owning warp substitutes the current token's
-        // row in shared memory and stores it to the cache.
-        if (ws >= tslot0 + wrow0 && ws < tslot0 + wrow0 + 16) {
-            const int row = ws - tslot0;
-            const int cg = lane & 15;
-            const bool is_v = lane >= 16;
-            if (cg < D / 8) {
-                const __nv_bfloat16* src = (is_v ? p.new_v : p.new_k) + static_cast<size_t>(u) * D;
-                const uint4 val = reinterpret_cast<const uint4*>(src)[cg];
-                *reinterpret_cast<uint4*>((is_v ? vb : kb) + swz_off(row, cg)) = val;
-                __nv_bfloat16* dst =
-                    (is_v ? p.v_cache : p.k_cache) + (static_cast<size_t>(u) * S + ws) * D;
-                reinterpret_cast<uint4*>(dst)[cg] = val;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
-
-        const int iA = tslot0 - slot0 + wrow0 + r;
-        const int iB = iA + 8;
-        const bool liveA = iA < n && ages[iA] >= 0;
-        const bool liveB = iB < n && ages[iB] >= 0;
-
-        // Logits S^T and row norms ||v||_1 for this warp's 16 slots.
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-        float nv[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-            const int lrow = wrow0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-            const uint32_t kbase = smem_u32(kb);
-            const uint32_t vbase = smem_u32(vb);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = swz_off(lrow, 2 * kk + (lane >> 4));
-                uint32_t a[4];
-                ldsm_x4(kbase + off, a);
-                mma_bf16_16816(sc, a, qf[kk][0], qf[kk][1]);
-                if constexpr (kScore) {
-                    uint32_t v[4];
-                    ldsm_x4(vbase + off, v);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) v[e] &= kAbsBf16x2;
-                    mma_bf16_16816(nv, v, kOnesBf16x2, kOnesBf16x2);
-                }
-            }
-        }
-
-        // Logits in the log2 domain; masked rows and padding heads -> -inf.
-        const float x0 = (liveA && hv0) ? sc[0] * sl : NEG;
-        const float x1 = (liveA && hv1) ? sc[1] * sl : NEG;
-        const float x2 = (liveB && hv0) ? sc[2] * sl : NEG;
-        const float x3 = (liveB && hv1) ? sc[3] * sl : NEG;
-
-        // Per-slot score terms t = log2(exp(s) * ||v||_1).
-        if (kScore && hv0) {
-            const int slotA = tslot0 + wrow0 + r;
-            float* st = p.stash + (static_cast<size_t>(u) * S + slotA) * G + h0;
-            if (liveA) {
-                const float lv = __log2f(nv[0]);
-                if (G == 1) st[0] = x0 + lv;
-                else *reinterpret_cast<float2*>(st) = make_float2(x0 + lv, x1 + lv);
-            }
-            if (liveB) {
-                const float lv = __log2f(nv[2]);
-                if (G == 1) st[8 * G] = x2 + lv;
-                else *reinterpret_cast<float2*>(st + 8 * G) = make_float2(x2 + lv, x3 + lv);
-            }
-        }
-
-        // Online softmax per head (columns h0, h0+1), across the warp's rows.
-        float mx0 = fmaxf(x0, x2);
-        float mx1 = fmaxf(x1, x3);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(m0, mx0);
-        const float mn1 = fmaxf(m1, mx1);
-        const float mu0 = (mn0 == NEG) ? 0.f : mn0;
-        const float mu1 = (mn1 == NEG) ? 0.f : mn1;
-        const float al0 = exp2f(m0 - mu0);
-        const float al1 = exp2f(m1 - mu1);
-        const float p0 = exp2f(x0 - mu0);
-        const float p1 = exp2f(x1 - mu1);
-        const float p2 = exp2f(x2 - mu0);
-        const float p3 = exp2f(x3 - mu1);
-        l0 = l0 * al0 + p0 + p2;
-        l1 = l1 * al1 + p1 + p3;
-        m0 = mn0;
-        m1 = mn1;
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-            acc[mt][0] *= al0;
-            acc[mt][1] *= al1;
-            acc[mt][2] *= al0;
-            acc[mt][3] *= al1;
-        }
-        // P^T (slots x heads) as the B operand of the P.V step.
-        const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-        const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
-
-        // V^T columns of masked slots are zeroed (select, never multiply).
-        const uint32_t bl = __ballot_sync(0xffffffffu, liveA);
-        const uint32_t bh = __ballot_sync(0xffffffffu, liveB);
-        const int k0 = 2 * (lane & 3);
-        const uint32_t mlo = (((bl >> (4 * k0)) & 1u) ? 0x0000ffffu : 0u) |
-                             (((bl >> (4 * k0 + 4)) & 1u) ? 0xffff0000u : 0u);
-        const uint32_t mhi = (((bh >> (4 * k0)) & 1u) ? 0x0000ffffu : 0u) |
-                             (((bh >> (4 * k0 + 4)) & 1u) ? 0xffff0000u : 0u);
-        {
-            const int lrow = wrow0 + (lane & 7) + (lane >> 4) * 8;
-            const uint32_t vbase = smem_u32(vb);
-#pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-                uint32_t a[4];
-                ldsm_x4_trans(vbase + swz_off(lrow, 2 * mt + ((lane >> 3) & 1)), a);
-                a[0] &= mlo;
-                a[1] &= mlo;
-                a[2] &= mhi;
-                a[3] &= mhi;
-                mma_bf16_16816(acc[mt], a, pb0, pb1);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-    }
-
-    // ------------------------------------------ merge the 4 warps' state --
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-    consumer_bar_sync();  // every consumer is done with the stage buffers
-    float* wO = reinterpret_cast<float*>(smem);  // [4][G][D]
-    float* wm = wO + kConsumerWarps * G * D;     // [4][G]
-    float* wl = wm + kConsumerWarps * G;         // [4][G]
-    if (r == 0) {
-        if (hv0) { wm[warp * G + h0] = m0; wl[warp * G + h0] = l0; }
-        if (hv1) { wm[warp * G + h0 + 1] = m1; wl[warp * G + h0 + 1] = l1; }
-    }
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-        const int dd = mt * 16 + r;
-        if (hv0) {
-            wO[(warp * G + h0) * D + dd] = acc[mt][0];
-            wO[(warp * G + h0) * D + dd + 8] = acc[mt][2];
-        }
-        if (hv1) {
-            wO[(warp * G + h0 + 1) * D + dd] = acc[mt][1];
-            wO[(warp * G + h0 + 1) * D + dd + 8] = acc[mt][3];
-        }
-    }
-    consumer_bar_sync();
-
-    if constexpr (kCluster) {
-        cluster_epilogue<D, G, kScore>(p, u, slot0, n, ages, smem, wO, wm, wl, cnt, tid);
-        return;
-    }
-
-    const size_t pidx = static_cast<size_t>(u) * p.nchunk + chunk;
-    if (cnt > 0) {
-        float* po = p.part_o + pidx * G * D;
-        for (int e = tid; e < G * D; e += kConsumers) {
-            const int h = e / D;
-            float mh = NEG;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) mh = fmaxf(mh, wm[w * G + h]);
-            float o = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float mw = wm[w * G + h];
-                if (mw != NEG) o += wO[w * G * D + e] * exp2f(mw - mh);
-            }
-            po[e] = o;
-        }
-    }
-    if (tid < G) {
-        float mh = NEG;
-        float l = 0.f;
-        if (cnt > 0) {
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) mh = fmaxf(mh, wm[w * G + tid]);
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float mw = wm[w * G + tid];
-                if (mw != NEG) l += wl[w * G + tid] * exp2f(mw - mh);
-            }
-        }
-        p.part_ml[pidx * G + tid] = make_float2(mh, l);
-    }
-
-    // ---------------------------------------- last CTA of the unit merges --
-    __threadfence();
-    consumer_bar_sync();
-    if (tid == 0) {
-        int last = 1;
-        if (p.nchunk > 1) {
-            const uint32_t prev = atomicAdd(&p.arrivals[u], 1u);
-            last = (prev == static_cast<uint32_t>(p.nchunk - 1));
-            if (last) p.arrivals[u] = 0u;  // every chunk of the unit has arrived
-        }
-        misc[2] = last;
-    }
-    consumer_bar_sync();
-    if (!misc[2]) return;
-    __threadfence();
-    finish_unit<D, G, kScore>(p, u, smem, L::kBarOff,
-                              reinterpret_cast<uint64_t*>(smem + L::kScanBarOff), tid);
-}
-
-template <int D, int G, int kStages, bool kScore, bool kCluster>
-cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
-                     int units, cudaStream_t stream, bool pdl) {
-    using L = StepSmem<D, kStages>;
-    if (finish_smem_bytes(p.nchunk, G, kScore ? p.topk : 1) > static_cast<size_t>(L::kBarOff))
-        return cudaErrorInvalidConfiguration;
-    auto kernel = lf_decode_step_kernel<D, G, kStages, kScore, kCluster>;
-    static int configured_for = -1;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (configured_for != dev) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-        if (e != cudaSuccess) return e;
-        configured_for = dev;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.nchunk, units);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = L::kAlloc;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    if (pdl) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
-    if constexpr (kCluster) {
-        attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = static_cast<unsigned>(p.nchunk);
-        attr[na].val.clusterDim.y = 1;
-        attr[na].val.clusterDim.z = 1;
-        ++na;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    e = cudaLaunchKernelEx(&cfg, kernel, tmK, tmV, p);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-}
 
 // ------------------------------------------------------ split finish --
 //
@@ -1405,11 +156,7 @@ __global__ void __launch_bounds__(kScoreThreads, G >= 8 ? 4 : 8) lf_score_kernel
 
 template <int D, int G>
 cudaError_t launch_dg(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
-                      int units, cudaStream_t stream, int stages, bool score, bool cluster,
-                      bool pdl) {
-    if (cluster)
-        return score ? launch_t<D, G, 2, true, true>(tmK, tmV, p, units, stream, pdl)
-                     : launch_t<D, G, 2, false, true>(tmK, tmV, p, units, stream, pdl);
+                      int units, cudaStream_t stream, int stages, bool score, bool pdl) {
     if (!score) return launch_t<D, G, 2, false, false>(tmK, tmV, p, units, stream, pdl);
     return stages == 2 ? launch_t<D, G, 2, true, false>(tmK, tmV, p, units, stream, pdl)
                        : launch_t<D, G, 3, true, false>(tmK, tmV, p, units, stream, pdl);
@@ -1454,7 +201,9 @@ cudaError_t launch_score_t(const StepParams& p, int units, cudaStream_t stream, 
 bool step_fits(int D, int G, int stages, bool score, int nchunk, int topk) {
     const size_t need = finish_smem_bytes(nchunk, G, score ? topk : 1);
     size_t have;
-    if (stages == 2 || !score)
+    if (stages == kDeepStages)
+        have = D == 64 ? StepSmem<64, kDeepStages>::kBarOff : StepSmem<128, kDeepStages>::kBarOff;
+    else if (stages == 2 || !score)
         have = D == 64 ? StepSmem<64, 2>::kBarOff : StepSmem<128, 2>::kBarOff;
     else
         have = D == 64 ? StepSmem<64, 3>::kBarOff : StepSmem<128, 3>::kBarOff;
@@ -1462,6 +211,8 @@ bool step_fits(int D, int G, int stages, bool score, int nchunk, int topk) {
 }
 
 size_t step_smem_bytes(int D, int stages) {
+    if (stages == kDeepStages)
+        return D == 64 ? StepSmem<64, kDeepStages>::kAlloc : StepSmem<128, kDeepStages>::kAlloc;
     if (stages == 2) return D == 64 ? StepSmem<64, 2>::kAlloc : StepSmem<128, 2>::kAlloc;
     return D == 64 ? StepSmem<64, 3>::kAlloc : StepSmem<128, 3>::kAlloc;
 }
@@ -1473,9 +224,10 @@ cudaError_t launch_decode_step(int D, int G, int stages, bool score, bool cluste
     // with the tail of the previous kernel in the stream (LF_PDL=0: off).
     const char* env = std::getenv("LF_PDL");
     const bool pdl = !(env && std::atoi(env) == 0);
+    if (cluster) return launch_decode_step_cluster(D, G, stages, score, tmK, tmV, p, units, stream, pdl);
 #define LF_STEP_CASE(DD, GG) \
     if (D == DD && G == GG)  \
-        return launch_dg<DD, GG>(tmK, tmV, p, units, stream, stages, score, cluster, pdl);
+        return launch_dg<DD, GG>(tmK, tmV, p, units, stream, stages, score, pdl);
     LF_STEP_CASE(64, 1) LF_STEP_CASE(64, 2) LF_STEP_CASE(64, 4) LF_STEP_CASE(64, 8)
     LF_STEP_CASE(128, 1) LF_STEP_CASE(128, 2) LF_STEP_CASE(128, 4) LF_STEP_CASE(128, 8)
 #undef LF_STEP_CASE

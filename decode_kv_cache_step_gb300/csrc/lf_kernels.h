@@ -52,6 +52,7 @@ constexpr int kFlagFillEmptyFirst = 1;  // empty (masked) slots are returned bef
 constexpr int kFlagMaskEvicted = 2;     // returned slots are masked (-1) in place
 constexpr int kMaxTopK = 1024;
 constexpr int kMaxClusterChunks = 8;    // chunks of a unit run as one cluster up to this
+constexpr int kDeepStages = 6;          // TMA ring of the one-CTA-per-SM cluster variant
 
 // Dynamic shared memory the kernel needs for head dim D and a TMA ring of
 // `stages` tiles (2 or 3).
@@ -69,6 +70,13 @@ bool step_fits(int D, int G, int stages, bool score, int nchunk, int topk);
 cudaError_t launch_decode_step(int D, int G, int stages, bool score, bool cluster,
                                const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const StepParams& p, int units, cudaStream_t stream);
+
+// The cluster instantiations (lf_decode_step_cluster.cu); stages is 2 or
+// kDeepStages.
+cudaError_t launch_decode_step_cluster(int D, int G, int stages, bool score,
+                                       const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                       const StepParams& p, int units, cudaStream_t stream,
+                                       bool pdl);
 
 // The scoring kernel of a split finish: grid (nchunk, units); CTA (c, u)
 // scores chunk c of unit u from the ages, the score terms and c_h, and the

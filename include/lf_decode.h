@@ -57,6 +57,9 @@
  *   LF_CHUNK_TILES=n   64-slot tiles per chunk of the slot axis (1..32)
  *   LF_STAGES=3        three-stage TMA ring (two CTAs per SM) instead of two
  *   LF_CLUSTER=0|1     thread-block-cluster merge off / on wherever it fits
+ *   LF_DEEP=0|1        cluster grids of at most one CTA per SM keep the
+ *                      2-stage TMA ring / take the deep one even for chunks
+ *                      of fewer than 5 tiles
  *   LF_PDL=0           programmatic dependent launch off
  *   LF_SPLIT=0|1       split finish off / on for every top-1 step without
  *                      clusters (default: units of at least 8192 slots)

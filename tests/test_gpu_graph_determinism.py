@@ -74,7 +74,8 @@ def test_cuda_graph_replay_equals_eager(name):
 
 
 @pytest.mark.parametrize("env", [{}, {"LF_PDL": "0"}, {"LF_CLUSTER": "0"}, {"LF_CLUSTER": "1"},
-                                 {"LF_STAGES": "3"}, {"LF_CLUSTER": "0", "LF_SPLIT": "1"},
+                                 {"LF_STAGES": "3"}, {"LF_CLUSTER": "1", "LF_DEEP": "0"},
+                                 {"LF_CLUSTER": "0", "LF_SPLIT": "1"},
                                  {"LF_CLUSTER": "0", "LF_SPLIT": "1", "LF_PDL": "0"}])
 def test_step_is_bitwise_deterministic(monkeypatch, env):
     for k, v in env.items():

@@ -93,10 +93,11 @@ def check_ex(case, W, scale, k, flags, where):
     return gpu, ora
 
 
-@pytest.mark.parametrize("cluster", ["1", "0"])
+@pytest.mark.parametrize("cluster,deep", [("1", "1"), ("1", "0"), ("0", "1")])
 @pytest.mark.parametrize("d,g,S", [(64, 1, 100), (128, 4, 300), (128, 8, 1000), (64, 2, 65)])
-def test_attention_only_matches_oracle(monkeypatch, d, g, S, cluster):
+def test_attention_only_matches_oracle(monkeypatch, d, g, S, cluster, deep):
     monkeypatch.setenv("LF_CLUSTER", cluster)
+    monkeypatch.setenv("LF_DEEP", deep)
     rng = np.random.default_rng(d + g + S)
     case = _pins.rand_case(rng, 2, 2 * g, 2, d, S, p_masked=0.3, max_age=3 * S, ws_mode="any")
     dc = _dev_case(case)
@@ -141,11 +142,13 @@ def test_topk_matches_oracle(k):
     check_ex(case, 16, 0.088, k, 0, f"k={k}")
 
 
-@pytest.mark.parametrize("cluster,split", [("1", "0"), ("0", "0"), ("0", "1")])
+@pytest.mark.parametrize("cluster,split,deep", [("1", "0", "1"), ("1", "0", "0"), ("0", "0", "1"),
+                                                ("0", "1", "1")])
 @pytest.mark.parametrize("k,flags", [(1, 1), (8, 1), (1, 2), (32, 2), (64, 3), (1, 3)])
-def test_fill_first_and_mask_evicted(monkeypatch, k, flags, cluster, split):
+def test_fill_first_and_mask_evicted(monkeypatch, k, flags, cluster, split, deep):
     monkeypatch.setenv("LF_CLUSTER", cluster)
     monkeypatch.setenv("LF_SPLIT", split)
+    monkeypatch.setenv("LF_DEEP", deep)
     rng = np.random.default_rng(600 + 10 * k + flags)
     case = _pins.rand_case(rng, 3, 4, 2, 64, 700, p_masked=0.05, max_age=3000)
     check_ex(case, 8, 0.125, k, flags, f"k={k} flags={flags}")

@@ -142,17 +142,28 @@ def test_host_io_entry_point_matches_device_entry_point(monkeypatch, io):
     assert torch.equal(a.mask, b.mask) and torch.equal(a.k, b.k)
 
 
-@pytest.mark.parametrize("cluster,split", [("1", "0"), ("0", "0"), ("0", "1")])
+@pytest.mark.parametrize("cluster,split,deep", [("1", "0", "1"), ("1", "0", "0"), ("0", "0", "1"),
+                                                ("0", "1", "1")])
 @pytest.mark.parametrize("chunk_tiles", ["1", "3", "32"])
-def test_split_shapes_do_not_change_results(monkeypatch, chunk_tiles, cluster, split):
-    """Different slot-axis splits, merged inside a thread-block cluster or by
-    the unit's last CTA (scoring there or in the split-finish kernel), give
-    results within tolerance of the oracle."""
+def test_split_shapes_do_not_change_results(monkeypatch, chunk_tiles, cluster, split, deep):
+    """Different slot-axis splits, merged inside a thread-block cluster (deep
+    or 2-stage TMA ring) or by the unit's last CTA (scoring there or in the
+    split-finish kernel), give results within tolerance of the oracle."""
     monkeypatch.setenv("LF_CHUNK_TILES", chunk_tiles)
     monkeypatch.setenv("LF_CLUSTER", cluster)
     monkeypatch.setenv("LF_SPLIT", split)
+    monkeypatch.setenv("LF_DEEP", deep)
     wl = WORKLOADS["long_b32_s16384_ragged"].with_batch(2)
     run_parity(wl, steps=2)
+
+
+@pytest.mark.parametrize("name", ["qwen3_8b_b1_s2400", "tiny_b2_s256"])
+def test_two_stage_cluster_path_every_step(monkeypatch, name):
+    """The cluster merge with the 2-stage TMA ring (grids of more than one CTA
+    per SM; the small workloads take the deep ring by default)."""
+    monkeypatch.setenv("LF_DEEP", "0")
+    wl = WORKLOADS[name]
+    run_parity(wl, min(wl.steps, 32))
 
 
 @pytest.mark.parametrize("split", ["0", "1"])

@@ -900,19 +900,24 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     // is issued before any store, so the chunk's mask costs one round trip.
     // The aged entries are stored evict-last: the next step reads them again,
     // and between the two the K/V stream passes through L2 evict-first.
-    constexpr int kPer = (kMaxChunkTiles * kTile + kThreads - 1) / kThreads;
+    // Only the consumer threads age: their fence before the unit's arrival
+    // counter (below) then also publishes the aged mask to the unit's last
+    // CTA, and no fence delays the start of the pipeline. (Cluster CTAs read
+    // ages from shared memory only.)
+    constexpr int kPer = (kMaxChunkTiles * kTile + kConsumers - 1) / kConsumers;
     int32_t* mrow = p.mask + static_cast<size_t>(u) * S + slot0;
     const uint64_t mask_pol = l2_policy_evict_last();
+    const bool ager = tid < kConsumers;
     int av[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-        const int i = tid + k * kThreads;
-        av[k] = (i < n) ? mrow[i] : -1;
+        const int i = tid + k * kConsumers;
+        av[k] = (ager && i < n) ? mrow[i] : -1;
     }
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-        const int i = tid + k * kThreads;
-        if (i < n) {
+        const int i = tid + k * kConsumers;
+        if (ager && i < n) {
             int a = av[k];
             if (ws >= 0) {
                 int na;
@@ -926,7 +931,6 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
             ages[i] = a;
         }
     }
-    __threadfence();  // the aged mask is read by the unit's last CTA
     __syncthreads();
 
     // Tiles with no live slot are never loaded (ragged fills stream only

@@ -870,8 +870,11 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     allow_dependent_launch();
     grid_dependency_wait();
 
+    // In the one-wave cluster variant (latency-bound) the write slot, q and
+    // the chunk's mask are all loaded before the slot is checked, so they
+    // share one round trip; large grids check it first (measured faster).
     int ws = p.write_slot[u];
-    if (ws < -1 || ws >= S) {
+    if (!kCluster && (ws < -1 || ws >= S)) {
         if (tid == 0 && chunk == 0) atomicOr(p.dev_err, LF_DEVERR_BAD_WRITE_SLOT);
         ws = -1;
     }
@@ -913,6 +916,10 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     for (int k = 0; k < kPer; ++k) {
         const int i = tid + k * kConsumers;
         av[k] = (ager && i < n) ? mrow[i] : -1;
+    }
+    if (kCluster && (ws < -1 || ws >= S)) {
+        if (tid == 0 && chunk == 0) atomicOr(p.dev_err, LF_DEVERR_BAD_WRITE_SLOT);
+        ws = -1;
     }
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {

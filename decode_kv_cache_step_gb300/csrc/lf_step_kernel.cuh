@@ -635,7 +635,7 @@ __host__ __device__ constexpr size_t finish_smem_bytes(int nchunk, int G, int to
 // its own chunk's slots, and rank 0 reduces the cluster's (I_j, j) argmin.
 // wO/wm/wl hold the four consumer warps' states (consumer threads only; the
 // producer warp joins the three cluster barriers on its own).
-template <int D, int G, bool kScore>
+template <int D, int G, int kStages, bool kScore>
 __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
                                  const int32_t* ages, uint8_t* smem, const float* wO,
                                  const float* wm, const float* wl, int cnt, int tid) {
@@ -654,6 +654,22 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
     int* red_j = reinterpret_cast<int*>(red_v + kConsumerWarps);             // [4]
     const float NEG = -INFINITY;
 
+    // This chunk's score terms (first batch) are requested first: they do
+    // not depend on the merge, so their round trip overlaps it (the
+    // consumers' barriers after the main loop ordered their stores).
+    constexpr int kBatch = 8;
+    // (Held across the merge only where registers allow: the deep ring runs
+    // one CTA per SM; the 2-stage ring at g = 8 would spill.)
+    constexpr bool kPreload = kScore && (G <= 4 || kStages == kDeepStages);
+    float t0[kBatch][G];
+    if constexpr (kPreload) {
+        const float* stash0 = p.stash + (static_cast<size_t>(u) * p.S + slot0) * G;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int i = tid + k * kConsumers;
+            if (i < n && ages[i] >= 0) load_terms<G>(stash0 + static_cast<size_t>(i) * G, t0[k]);
+        }
+    }
     // This chunk's merged state, published for the cluster.
     for (int e = tid; e < G * D; e += kConsumers) {
         const int h = e / D;
@@ -740,16 +756,26 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
         const float* stash = p.stash + static_cast<size_t>(u) * S * G;
         float* scores = p.scores ? p.scores + static_cast<size_t>(u) * S : nullptr;
         const bool fill_first = (p.flags & kFlagFillEmptyFirst) != 0;
-        float best = INFINITY;
+        const int W = p.W;
+        // A thread visits its slots in increasing order, so a strict "<" on
+        // the key (score bits + 1; 0 for an empty slot under fill-empty-first)
+        // keeps the lowest slot among equal keys.
+        uint32_t bkey = 0xffffffffu;
         int bestj = 0x7fffffff;
-        constexpr int kBatch = 8;
         for (int i0 = tid; i0 < n; i0 += kBatch * kConsumers) {
             float t[kBatch][G];
+            if (kPreload && i0 == tid) {
 #pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int i = i0 + k * kConsumers;
-                if (i < n && ages[i] >= 0)
-                    load_terms<G>(stash + static_cast<size_t>(slot0 + i) * G, t[k]);
+                for (int k = 0; k < kBatch; ++k)
+#pragma unroll
+                    for (int h = 0; h < G; ++h) t[k][h] = t0[k][h];
+            } else {
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    const int i = i0 + k * kConsumers;
+                    if (i < n && ages[i] >= 0)
+                        load_terms<G>(stash + static_cast<size_t>(slot0 + i) * G, t[k]);
+                }
             }
 #pragma unroll
             for (int k = 0; k < kBatch; ++k) {
@@ -757,26 +783,22 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
                 if (i >= n) break;
                 const int a = ages[i];
                 const int j = slot0 + i;
-                float I = INFINITY;
-                bool cand = false;
-                float cval = 0.f;
-                if (a >= 0) {
-                    I = 0.f;
+                float I = 0.f;
 #pragma unroll
-                    for (int h = 0; h < G; ++h) I += ex2_approx(t[k][h] + cexp[h]);
-                    cand = a >= p.W && !isnan(I);
-                    cval = I;
-                } else if (fill_first) {
-                    cand = true;
-                    cval = -1.f;
-                }
-                if (cand && better(cval, j, best, bestj)) {
-                    best = cval;
+                for (int h = 0; h < G; ++h) I += ex2_approx(t[k][h] + cexp[h]);
+                const bool live = a >= 0;
+                const bool cand = live ? (a >= W && I == I) : fill_first;
+                const uint32_t key = live ? __float_as_uint(I) + 1u : 0u;
+                if (cand && key < bkey) {
+                    bkey = key;
                     bestj = j;
                 }
-                if (scores) scores[j] = I;
+                if (scores) scores[j] = live ? I : INFINITY;
             }
         }
+        // Back to the (value, slot) form the cluster's reduction compares.
+        float best = bkey == 0xffffffffu ? INFINITY
+                                         : (bkey == 0u ? -1.f : __uint_as_float(bkey - 1u));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float ov = __shfl_xor_sync(0xffffffffu, best, off);
@@ -1174,7 +1196,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     consumer_bar_sync();
 
     if constexpr (kCluster) {
-        cluster_epilogue<D, G, kScore>(p, u, slot0, n, ages, smem, wO, wm, wl, cnt, tid);
+        cluster_epilogue<D, G, kStages, kScore>(p, u, slot0, n, ages, smem, wO, wm, wl, cnt, tid);
         return;
     }
 

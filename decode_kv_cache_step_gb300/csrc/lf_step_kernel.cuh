@@ -304,48 +304,100 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int usabl
     uint8_t* scan_area = topk_area + (p.topk > 1 ? kTopKAreaBytes : 0);
     const int scan_bytes = usable - static_cast<int>(scan_area - smem);
     const float2* ml = p.part_ml + static_cast<size_t>(u) * nchunk * G;
-
-    if (tid < G) {
-        float m = -INFINITY;
-        for (int c = 0; c < nchunk; ++c) m = fmaxf(m, __ldcg(&ml[c * G + tid]).x);
-        float l = 0.f;
-        for (int c = 0; c < nchunk; ++c) {
-            const float2 v = __ldcg(&ml[c * G + tid]);
-            if (v.x != -INFINITY) l += v.y * exp2f(v.x - m);
-        }
-        s_m[tid] = m;
-        s_il[tid] = (l > 0.f) ? 1.f / l : 0.f;
-    }
-    if (tid == 0) s_ncand[0] = 0;
-    consumer_bar_sync();
-    for (int e = tid; e < nchunk * G; e += kConsumers) {
-        const float2 v = __ldcg(&ml[e]);
-        const int h = e % G;
-        s_w[e] = (v.x == -INFINITY) ? 0.f : exp2f(v.x - s_m[h]) * s_il[h];
-        if (h == 0) s_live[e / G] = v.x != -INFINITY;  // m = -inf: no live slot
-    }
-    consumer_bar_sync();
-
-    // Output: O_h = sum_c w_ch * O_ch, rounded to bf16.
     const int b = u / p.Hkv;
     const int kvh = u - b * p.Hkv;
     const float* po = p.part_o + static_cast<size_t>(u) * nchunk * G * D;
     __nv_bfloat16* out = p.out + (static_cast<size_t>(b) * p.Hq + kvh * G) * D;
-    // Loads of four chunks are issued together; a chunk that had no live
-    // tile has weight 0 and its (unwritten) partial is selected away.
+
+    // The partial outputs of the first four chunks are requested first: they
+    // do not depend on (m, l), so their round trip overlaps the weights'.
     constexpr int kPerT = (G * D + kConsumers - 1) / kConsumers;
+    float v0[4][kPerT];
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        const int c = min(cc, nchunk - 1);
+#pragma unroll
+        for (int k = 0; k < kPerT; ++k) {
+            const int e = tid + k * kConsumers;
+            v0[cc][k] = (e < G * D) ? __ldcg(&po[static_cast<size_t>(c) * G * D + e]) : 0.f;
+        }
+    }
+
+    // Per head: m = max_c m_c, l = sum_c l_c 2^(m_c - m), weights
+    // w_c = 2^(m_c - m) / l. Up to kFastChunks chunks thread h loads all of
+    // its head's (m_c, l_c) at once and writes the weights itself.
+    constexpr int kFastChunks = 16;
+    const bool fast = nchunk <= kFastChunks;
+    if (tid < G) {
+        if (fast) {
+            float2 mlv[kFastChunks];
+#pragma unroll
+            for (int c = 0; c < kFastChunks; ++c)
+                if (c < nchunk) mlv[c] = __ldcg(&ml[c * G + tid]);
+            float m = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kFastChunks; ++c)
+                if (c < nchunk) m = fmaxf(m, mlv[c].x);
+            float l = 0.f;
+#pragma unroll
+            for (int c = 0; c < kFastChunks; ++c)
+                if (c < nchunk && mlv[c].x != -INFINITY) l += mlv[c].y * exp2f(mlv[c].x - m);
+            const float il = (l > 0.f) ? 1.f / l : 0.f;
+            s_m[tid] = m;
+            s_il[tid] = il;
+#pragma unroll
+            for (int c = 0; c < kFastChunks; ++c) {
+                if (c < nchunk) {
+                    s_w[c * G + tid] = (mlv[c].x == -INFINITY) ? 0.f : exp2f(mlv[c].x - m) * il;
+                    if (tid == 0) s_live[c] = mlv[c].x != -INFINITY;  // m = -inf: no live slot
+                }
+            }
+        } else {
+            float m = -INFINITY;
+            for (int c = 0; c < nchunk; ++c) m = fmaxf(m, __ldcg(&ml[c * G + tid]).x);
+            float l = 0.f;
+            for (int c = 0; c < nchunk; ++c) {
+                const float2 v = __ldcg(&ml[c * G + tid]);
+                if (v.x != -INFINITY) l += v.y * exp2f(v.x - m);
+            }
+            s_m[tid] = m;
+            s_il[tid] = (l > 0.f) ? 1.f / l : 0.f;
+        }
+    }
+    if (tid == 0) s_ncand[0] = 0;
+    consumer_bar_sync();
+    if (!fast) {
+        for (int e = tid; e < nchunk * G; e += kConsumers) {
+            const float2 v = __ldcg(&ml[e]);
+            const int h = e % G;
+            s_w[e] = (v.x == -INFINITY) ? 0.f : exp2f(v.x - s_m[h]) * s_il[h];
+            if (h == 0) s_live[e / G] = v.x != -INFINITY;  // m = -inf: no live slot
+        }
+        consumer_bar_sync();
+    }
+
+    // Output: O_h = sum_c w_ch * O_ch, rounded to bf16. Four chunks' loads
+    // are in flight at a time; a chunk that had no live tile has weight 0 and
+    // its (unwritten) partial is selected away.
     float o[kPerT];
 #pragma unroll
     for (int k = 0; k < kPerT; ++k) o[k] = 0.f;
     for (int c0 = 0; c0 < nchunk; c0 += 4) {
         float v[4][kPerT];
+        if (c0 == 0) {
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const int c = min(c0 + cc, nchunk - 1);
+            for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-            for (int k = 0; k < kPerT; ++k) {
-                const int e = tid + k * kConsumers;
-                v[cc][k] = (e < G * D) ? __ldcg(&po[static_cast<size_t>(c) * G * D + e]) : 0.f;
+                for (int k = 0; k < kPerT; ++k) v[cc][k] = v0[cc][k];
+        } else {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c = min(c0 + cc, nchunk - 1);
+#pragma unroll
+                for (int k = 0; k < kPerT; ++k) {
+                    const int e = tid + k * kConsumers;
+                    v[cc][k] = (e < G * D) ? __ldcg(&po[static_cast<size_t>(c) * G * D + e]) : 0.f;
+                }
             }
         }
 #pragma unroll

@@ -614,8 +614,9 @@ __device__ void score_and_select(const StepParams& p, int u, const float* s_m, c
         }
     } else {
         // Batches of loads in flight per thread (also for slot counts that
-        // break the 16-byte copy alignment).
-        constexpr int kBatch = 8;
+        // break the 16-byte copy alignment): 13 per thread covers a
+        // 3200-slot unit in two round trips without spilling (g <= 4).
+        constexpr int kBatch = G <= 4 ? 13 : 8;
         for (int j0 = tid; j0 < S; j0 += kBatch * kConsumers) {
             int a[kBatch];
             float t[kBatch][G];

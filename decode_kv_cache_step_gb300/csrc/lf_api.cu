@@ -378,7 +378,7 @@ lf_status check_args(const StepArgs& a, const Shape& s) {
 }
 
 struct Layout {
-    size_t ml, o, stash, cfold, total;
+    size_t ml, o, stash, cfold, tiles, total;
 };
 
 Layout scratch_layout(const Shape& s, const Plan& pl, size_t extra) {
@@ -389,7 +389,8 @@ Layout scratch_layout(const Shape& s, const Plan& pl, size_t extra) {
     L.o = align_up(L.ml + units * pl.nchunk * g * sizeof(float2), 256);
     L.stash = align_up(L.o + units * pl.nchunk * g * s.d * sizeof(float), 256);
     L.cfold = align_up(L.stash + units * static_cast<size_t>(s.S) * g * sizeof(float), 256);
-    L.total = align_up(L.cfold + units * g * sizeof(float), 256) + extra;
+    L.tiles = align_up(L.cfold + units * g * sizeof(float), 256);
+    L.total = align_up(L.tiles + units * pl.nchunk * sizeof(uint32_t), 256) + extra;
     return L;
 }
 
@@ -421,6 +422,7 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
     sp.arrivals = scr->arrivals;
     sp.dev_err = scr->dev_err;
     sp.cfold = reinterpret_cast<float*>(base + L.cfold);
+    sp.part_tiles = reinterpret_cast<uint32_t*>(base + L.tiles);
     sp.score_arrivals = scr->arrivals + units;
     sp.best = reinterpret_cast<unsigned long long*>(scr->arrivals + 2 * static_cast<size_t>(units));
     sp.Hq = s.Hq;

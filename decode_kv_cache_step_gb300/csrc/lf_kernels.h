@@ -31,6 +31,9 @@ struct StepParams {
     // scratch
     float* part_o;               // [units][nchunk][G][D]  unnormalised output, base m
     float2* part_ml;             // [units][nchunk][G]     (m, l), log2 domain
+    // [units][nchunk]: bit t set when tile t of the chunk holds a live slot
+    // (written by the chunk's CTA; nullptr: not kept)
+    uint32_t* part_tiles = nullptr;
     float* stash;                // [units][S][G]          log2(exp(s) * ||v||_1) per live slot
     uint32_t* arrivals;          // [units] chunk arrival counters, 0 between steps
     uint32_t* dev_err;           // LF_DEVERR_* bits

@@ -323,6 +323,13 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int usabl
         }
     }
 
+    // Chunk liveness for the score scan: the chunks' live-tile masks when
+    // they were kept (0: no live slot), else from m_c below.
+    // (Loaded into a register now, stored after the (m, l) loads are issued.)
+    const uint32_t* ptl =
+        (p.part_tiles && !p.split) ? p.part_tiles + static_cast<size_t>(u) * nchunk : nullptr;
+    const uint32_t my_tiles = (kScore && ptl && tid < nchunk) ? __ldcg(&ptl[tid]) : 0u;
+
     // Per head: m = max_c m_c, l = sum_c l_c 2^(m_c - m), weights
     // w_c = 2^(m_c - m) / l. Up to kFastChunks chunks thread h loads all of
     // its head's (m_c, l_c) at once and writes the weights itself.
@@ -349,7 +356,8 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int usabl
             for (int c = 0; c < kFastChunks; ++c) {
                 if (c < nchunk) {
                     s_w[c * G + tid] = (mlv[c].x == -INFINITY) ? 0.f : exp2f(mlv[c].x - m) * il;
-                    if (tid == 0) s_live[c] = mlv[c].x != -INFINITY;  // m = -inf: no live slot
+                    if (tid == 0 && !(kScore && ptl))
+                        s_live[c] = mlv[c].x != -INFINITY ? -1 : 0;  // m = -inf: no live slot
                 }
             }
         } else {
@@ -364,6 +372,11 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int usabl
             s_il[tid] = (l > 0.f) ? 1.f / l : 0.f;
         }
     }
+    if (kScore && ptl) {
+        if (tid < nchunk) s_live[tid] = static_cast<int>(my_tiles);
+        for (int c = tid + kConsumers; c < nchunk; c += kConsumers)
+            s_live[c] = static_cast<int>(__ldcg(&ptl[c]));
+    }
     if (tid == 0) s_ncand[0] = 0;
     consumer_bar_sync();
     if (!fast) {
@@ -371,7 +384,8 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int usabl
             const float2 v = __ldcg(&ml[e]);
             const int h = e % G;
             s_w[e] = (v.x == -INFINITY) ? 0.f : exp2f(v.x - s_m[h]) * s_il[h];
-            if (h == 0) s_live[e / G] = v.x != -INFINITY;  // m = -inf: no live slot
+            if (h == 0 && !(kScore && ptl))
+                s_live[e / G] = v.x != -INFINITY ? -1 : 0;  // m = -inf: no live slot
         }
         consumer_bar_sync();
     }
@@ -468,6 +482,8 @@ __device__ __forceinline__ void seg_advance(SegWalk& w, int cs, int seg, int S, 
 
 // Units with more slots to score than this stream them through shared memory.
 constexpr int kBulkScanMinSlots = 4096;
+// The live-tile list of the top-1 register scan holds at most this many tiles.
+constexpr int kMaxScanTiles = 1024;
 
 // LongFlowScore of every live slot of unit u and the selection of the slots to
 // evict, by the unit's last CTA once the final (m_h, l_h) are known.
@@ -540,7 +556,11 @@ __device__ void score_and_select(const StepParams& p, int u, const float* s_m, c
     // Short units are cheaper with loads batched in registers (one or two
     // round trips); long ones stream through shared memory.
     int nlive = 0;
-    for (int c = 0; c < nchunk; ++c) nlive += (all || s_live[c]) ? 1 : 0;
+    int live_tiles = 0;  // (from the live-tile masks when they were kept)
+    for (int c = 0; c < nchunk; ++c) {
+        nlive += (all || s_live[c]) ? 1 : 0;
+        live_tiles += __popc(static_cast<uint32_t>(s_live[c]));
+    }
     const bool bulk = seg >= kConsumers && nlive * cs > kBulkScanMinSlots && (S & 3) == 0 &&
                       (reinterpret_cast<uintptr_t>(p.mask) & 15) == 0;
     if (bulk) {
@@ -611,6 +631,48 @@ __device__ void score_and_select(const StepParams& p, int u, const float* s_m, c
             consumer_bar_sync();  // everyone is done with buffer b
             if (tid == 0 && wi.j0 < S) issue(issued++);
             seg_advance(wc, cs, seg, S, nchunk, s_live, all);
+        }
+    } else if (top1 && !all && p.part_tiles && nlive * p.chunk_tiles <= kMaxScanTiles &&
+               live_tiles < (S + kTile - 1) / kTile) {
+        // Top-1 over live tiles only, when some tile holds no live slot: the
+        // chunks' live-tile masks are expanded into a list of tile indices,
+        // and the batches walk the slots of the listed tiles (a ragged unit
+        // scans its live part, not all S slots). A thread still visits its
+        // slots in increasing order.
+        constexpr int kBatch = 8;
+        int* s_tl = reinterpret_cast<int*>(
+            (reinterpret_cast<uintptr_t>(scan_area) + 15) & ~static_cast<uintptr_t>(15));
+        if (tid < 32) {
+            int nt = 0;
+            for (int c = 0; c < nchunk; ++c) {
+                const uint32_t bits = static_cast<uint32_t>(s_live[c]);
+                if (!bits) continue;
+                if (tid < p.chunk_tiles && ((bits >> tid) & 1u))
+                    s_tl[nt + __popc(bits & ((1u << tid) - 1u))] = c * p.chunk_tiles + tid;
+                nt += __popc(bits);
+            }
+            if (tid == 0) s_ncand[1] = nt;
+        }
+        consumer_bar_sync();
+        const int nslots = s_ncand[1] * kTile;
+        for (int i0 = tid; i0 < nslots; i0 += kBatch * kConsumers) {
+            int a[kBatch];
+            int jj[kBatch];
+            float t[kBatch][G];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int i = i0 + k * kConsumers;
+                jj[k] = (i < nslots) ? s_tl[i >> 6] * kTile + (i & (kTile - 1)) : S;
+                a[k] = (jj[k] < S) ? __ldcg(&age[jj[k]]) : -1;
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k)
+                if (jj[k] < S) load_terms<G>(stash + static_cast<size_t>(jj[k]) * G, t[k]);
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (jj[k] >= S) break;
+                visit(jj[k], a[k], t[k]);
+            }
         }
     } else {
         // Batches of loads in flight per thread (also for slot counts that
@@ -1017,18 +1079,26 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
 
     // Tiles with no live slot are never loaded (ragged fills stream only
     // their live part).
+    // The same list, as a bit mask, tells the unit's last CTA which tiles
+    // its score scan can skip.
     if (warp == 0) {
         int cnt = 0;
+        uint32_t bits = 0u;
         for (int t = 0; t < ntiles; ++t) {
             const int i0 = t * kTile + lane;
             const int i1 = i0 + 32;
             const bool live = (i0 < n && ages[i0] >= 0) || (i1 < n && ages[i1] >= 0);
             if (__any_sync(0xffffffffu, live)) {
                 if (lane == 0) list[cnt] = t;
+                bits |= 1u << t;
                 ++cnt;
             }
         }
-        if (lane == 0) misc[0] = cnt;
+        if (lane == 0) {
+            misc[0] = cnt;
+            if (kScore && !kCluster && p.part_tiles && !p.split)
+                p.part_tiles[static_cast<size_t>(u) * p.nchunk + chunk] = bits;
+        }
     }
     __syncthreads();
     const int cnt = misc[0];

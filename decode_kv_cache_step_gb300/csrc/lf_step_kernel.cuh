@@ -40,9 +40,10 @@
 // (cache-fill phase) and the chosen slots can be masked in place.
 // Long units stream their score terms through shared memory with bulk copies
 // for that scan, or, for top-1 steps over units of thousands of slots, leave
-// the scan to a second kernel (the split finish, lf_score_kernel) that scores
-// every chunk of every unit in parallel once the step's memory traffic is
-// over. When the whole grid fits in one wave, a unit's chunks run as
+// the scan to a second kernel (the split finish, lf_score_kernel in
+// lf_decode_step.cu) that scores every chunk of every unit in parallel once
+// the step's memory traffic is over. Shorter ragged units scan only the tiles
+// that hold a live slot (top-1; the chunk CTAs publish their live-tile masks). When the whole grid fits in one wave, a unit's chunks run as
 // one thread-block cluster instead (kCluster): they merge through distributed
 // shared memory and each CTA scores its own chunk (top-1 only). A cluster
 // grid of at most one CTA per SM uses a kDeepStages-deep TMA ring, so every
@@ -298,7 +299,9 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int usabl
     float* red_v = s_il + G;                      // [4]
     int* red_j = reinterpret_cast<int*>(red_v + kConsumerWarps);
     int* s_ncand = red_j + kConsumerWarps;
-    int* s_live = s_ncand + 4;                    // [nchunk]: 1 if the chunk has a live slot
+    // [nchunk]: the chunk's live-tile bit mask (0: no live slot; all ones
+    // when the masks were not kept)
+    int* s_live = s_ncand + 4;
     uint8_t* topk_area = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(s_live + nchunk) + 15) & ~static_cast<uintptr_t>(15));
     uint8_t* scan_area = topk_area + (p.topk > 1 ? kTopKAreaBytes : 0);

@@ -247,10 +247,12 @@ constexpr int kSplitMinSlots = 8192;
 
 // Split the slot axis of every unit into nchunk chunks of chunk_tiles tiles.
 // Each CTA costs a fixed start-up and merge, so chunks stay long (13 to 32
-// tiles) as long as the grid still has about 3000 CTAs, about 20 per SM, to
-// balance the tail; a batch too small to fill the GPU that way uses short
-// chunks of about 5 tiles instead. At most kMaxChunkTiles tiles and
-// kMaxNChunk chunks.
+// tiles) while the grid still has about 27 CTAs per SM (about 4100), the
+// chunk count rounded down, to balance the tail (measured: 4 chunks of 13
+// tiles beat 3 of 17 on the Fig. 1 shape by 1 us per step, 2 chunks of 19
+// beat 3 of 13 on the 2400-slot ragged batch); a batch too small to fill
+// the GPU that way uses short chunks of about 5 tiles instead. At most
+// kMaxChunkTiles tiles and kMaxNChunk chunks.
 Plan plan_split(int S, int units, int sms, bool want_cluster) {
     Plan pl;
     pl.tiles = (S + lf::kTile - 1) / lf::kTile;
@@ -261,7 +263,7 @@ Plan plan_split(int S, int units, int sms, bool want_cluster) {
     }
     if (nchunk == 0) {
         const int longest = (pl.tiles + lf::kMaxChunkTiles - 1) / lf::kMaxChunkTiles;
-        const int fill = static_cast<int>((20L * sms + units - 1) / units);
+        const int fill = static_cast<int>((27L * sms) / units);
         if (static_cast<long>(units) * longest >= sms)
             nchunk = std::max(longest, std::min(fill, (pl.tiles + 12) / 13));
         else

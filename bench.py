@@ -43,7 +43,8 @@ from decode_kv_cache_step_gb300.workloads import (  # noqa: E402
 METRIC = "decode steps/s and achieved HBM GB/s (% of GB300 peak) for fused attn+score+evict"
 DEFAULT_WORKLOAD = "qwen3_8b_b128_s3200"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "lf_decode_step_kernel.qwen3_8b_b128_s3200.md")
+PROFILE_WORKLOAD = "qwen3_8b_b128_s3200"   # the workload the committed DRAM counters cover
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", f"lf_decode_step_kernel.{PROFILE_WORKLOAD}.md")
 KERNEL_SOURCES = ["lf_step_kernel.cuh", "lf_decode_step.cu", "lf_decode_step_cluster.cu",
                   "lf_ptx.cuh", "lf_kernels.h"]
 
@@ -530,7 +531,10 @@ def bench_lf(args, wl):
         "roofline": {"kernel": "lf_decode_step_kernel" + (" + lf_score_kernel" if split else ""),
                      "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": committed_traffic() if L == 1 and not split else None,
+                     # the committed counters cover one full-batch launch of one workload
+                     "traffic": (committed_traffic() if L == 1 and not split and world == 1
+                                 and wl.name == PROFILE_WORKLOAD and args.batch is None
+                                 else None),
                      "algorithmic_bytes_per_launch": alg_launch,
                      "avg_launch_ms": kern_avg_ms, "launches": kern_n,
                      "score_kernel_avg_ms": score_ms / max(kern_n, 1) if split else None,

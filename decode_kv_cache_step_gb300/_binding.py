@@ -230,8 +230,9 @@ def decode_attention(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, s
 
 def decode_step_host(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slot, W,
                      scale, stream=None):
-    """lf_decode_step_host: per-step I/O in host tensors (pinned for async copies),
-    caches and mask on the device. Outputs are valid after the stream syncs."""
+    """lf_decode_step_host: per-step I/O in host tensors, caches and mask on the
+    device. Pinned tensors are read and written by the kernel in place; others
+    are staged through device memory. Outputs are valid after the stream syncs."""
     lib = load_library()
     B, Hq, Hkv, d, S = _check_step(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out,
                                    next_slot, io_on_device=False)

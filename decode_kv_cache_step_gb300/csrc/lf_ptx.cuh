@@ -190,6 +190,14 @@ __device__ __forceinline__ int ld_dsmem_s32(uint32_t a) {
     return v;
 }
 
+__device__ __forceinline__ void st_dsmem_f32(uint32_t a, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_dsmem_s32(uint32_t a, int v) {
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
 // ------------------------------------------------------- warp MMA fragments --
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {

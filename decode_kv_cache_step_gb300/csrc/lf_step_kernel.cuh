@@ -750,9 +750,11 @@ __host__ __device__ constexpr size_t finish_smem_bytes(int nchunk, int G, int to
 // chunk). The chunk's merged (m, l, O) stay in shared memory; after a
 // cluster barrier every CTA reads its peers' through distributed shared
 // memory. CTA r writes its slice of the output row, every CTA scores only
-// its own chunk's slots, and rank 0 reduces the cluster's (I_j, j) argmin.
-// wO/wm/wl hold the four consumer warps' states (consumer threads only; the
-// producer warp joins the three cluster barriers on its own).
+// its own chunk's slots and writes its local best into rank 0's shared
+// memory, and rank 0 reduces the cluster's (I_j, j) argmin after the second
+// (last) cluster barrier. wO/wm/wl hold the four consumer warps' states
+// (consumer threads only; the producer warp joins the two cluster barriers
+// on its own).
 template <int D, int G, int kStages, bool kScore>
 __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
                                  const int32_t* ages, uint8_t* smem, const float* wO,
@@ -762,9 +764,10 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
     constexpr int kWBytes = (kConsumerWarps * G * D + 2 * kConsumerWarps * G) * 4;
     float* pub_o = reinterpret_cast<float*>(smem + ((kWBytes + 15) & ~15));  // [G][D]
     float2* pub_ml = reinterpret_cast<float2*>(pub_o + G * D);               // [G]
-    float* pub_best = reinterpret_cast<float*>(pub_ml + G);                  // [1]
-    int* pub_bestj = reinterpret_cast<int*>(pub_best + 1);                   // [1]
-    float2* s_mlc = reinterpret_cast<float2*>(pub_bestj + 3);                // [nchunk][G]
+    // Every CTA's local best, written into rank 0's copy of these arrays.
+    float* pub_best = reinterpret_cast<float*>(pub_ml + G);                  // [8]
+    int* pub_bestj = reinterpret_cast<int*>(pub_best + kMaxClusterChunks);   // [8]
+    float2* s_mlc = reinterpret_cast<float2*>(pub_bestj + kMaxClusterChunks);  // [nchunk][G]
     float* s_w = reinterpret_cast<float*>(s_mlc + kMaxClusterChunks * G);    // [nchunk][G]
     float* s_m = s_w + kMaxClusterChunks * G;                               // [G]
     float* s_il = s_m + G;                                                   // [G]
@@ -937,24 +940,25 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
                     best = red_v[w];
                     bestj = red_j[w];
                 }
-            *pub_best = best;
-            *pub_bestj = bestj;
+            st_dsmem_f32(dsmem_addr(&pub_best[rank], 0u), best);
+            st_dsmem_s32(dsmem_addr(&pub_bestj[rank], 0u), bestj);
         }
         // This chunk's score terms are read: drop them from L2, no write-back.
         discard_range(stash + static_cast<size_t>(slot0) * G, static_cast<size_t>(n) * G * 4, tid,
                       kConsumers);
     }
-    cluster_sync();  // #2: every output slice is written, every local best published
+    // #2: every peer's reads of this CTA's shared memory are done and every
+    // local best sits in rank 0's arrays; after it no CTA touches another's
+    // shared memory, so each may leave.
+    cluster_sync();
 
     if (kScore && rank == 0 && tid == 0) {
         float best = INFINITY;
         int bestj = 0x7fffffff;
         for (int c = 0; c < nchunk; ++c) {
-            const float v = ld_dsmem_f32(dsmem_addr(pub_best, static_cast<uint32_t>(c)));
-            const int j = ld_dsmem_s32(dsmem_addr(pub_bestj, static_cast<uint32_t>(c)));
-            if (better(v, j, best, bestj)) {
-                best = v;
-                bestj = j;
+            if (better(pub_best[c], pub_bestj[c], best, bestj)) {
+                best = pub_best[c];
+                bestj = pub_bestj[c];
             }
         }
         const int slot = (bestj == 0x7fffffff) ? -1 : bestj;
@@ -962,7 +966,6 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
         if (slot >= 0 && (p.flags & kFlagMaskEvicted))
             p.mask[static_cast<size_t>(u) * p.S + slot] = -1;
     }
-    cluster_sync();  // #3: no CTA leaves while a peer may still read its memory
 }
 
 // kStages-deep TMA ring; 3 stages run 2 CTAs per SM, 2 stages run 3.
@@ -1136,8 +1139,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         }
         if constexpr (kCluster) {
             __syncwarp();
-            cluster_sync();  // the consumers' cluster barriers #1, #2, #3
-            cluster_sync();
+            cluster_sync();  // the consumers' cluster barriers #1 and #2
             cluster_sync();
         }
         return;

@@ -16,4 +16,4 @@ from ._binding import (  # noqa: F401
     LF_STEP_FILL_EMPTY_FIRST, LF_STEP_MASK_EVICTED, LFError, decode_attention, decode_step, decode_step_ex,
     decode_step_host, decode_step_noalloc,
     decode_step_scores, device_errors, library_path, load_library, profile_collect,
-    profile_enable, release_workspace, status_string, version)
+    profile_enable, release_workspace, status_string, step_plan, version)

@@ -39,7 +39,7 @@ LF_MAX_TOPK = 1024
 # Every exported symbol of include/lf_decode.h.
 EXPORTED = (
     "lf_decode_step", "lf_decode_step_scores", "lf_decode_step_ex", "lf_decode_attention",
-    "lf_decode_step_host", "lf_decode_step_noalloc", "lf_device_errors",
+    "lf_decode_step_host", "lf_decode_step_noalloc", "lf_step_plan", "lf_device_errors",
     "lf_profile_enable", "lf_profile_collect", "lf_release_workspace", "lf_status_string",
     "lf_last_error", "lf_version",
 )
@@ -89,6 +89,8 @@ def load_library(path: str | None = None):
         lib.lf_decode_attention.restype = I
         for fn in (lib.lf_decode_step, lib.lf_decode_step_host, lib.lf_decode_step_scores):
             fn.restype = I
+        lib.lf_step_plan.argtypes = [I] * 6 + [ctypes.POINTER(ctypes.c_int32)]
+        lib.lf_step_plan.restype = I
         lib.lf_device_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I]
         lib.lf_device_errors.restype = I
         lib.lf_profile_enable.argtypes = [I]
@@ -254,6 +256,15 @@ def decode_step_noalloc(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), mask.data_ptr(), new_k.data_ptr(),
         new_v.data_ptr(), write_slot.data_ptr(), out.data_ptr(), next_slot.data_ptr(),
         B, Hq, Hkv, d, S, int(W), float(scale), _stream_handle(stream)))
+
+
+def step_plan(B: int, Hq: int, Hkv: int, d: int, S: int, topk: int = 1) -> dict:
+    """The launch plan a step of this shape takes on the current device."""
+    lib = load_library()
+    plan = (ctypes.c_int32 * 6)()
+    _check(lib, lib.lf_step_plan(int(B), int(Hq), int(Hkv), int(d), int(S), int(topk), plan))
+    return {"nchunk": plan[0], "chunk_tiles": plan[1], "stages": plan[2],
+            "cluster": bool(plan[3]), "split": bool(plan[4]), "cluster_fit": plan[5]}
 
 
 def device_errors(stream=None, clear: bool = True) -> int:

@@ -240,10 +240,20 @@ struct Plan {
     int tiles, chunk_tiles, nchunk, stages;
     bool cluster;  // the unit's chunks run as one thread-block cluster
     bool split;    // a top-1 step scores in a second kernel (split finish)
+    int fit = 0;   // clusters of the first size tried that can be resident at once
+                   // (-1: clusters not considered)
 };
 
 // Units of at least this many slots take the split finish.
 constexpr int kSplitMinSlots = 8192;
+
+// Largest cluster by default: 16 CTAs, a non-portable size (measured: the
+// 3200-slot Qwen3 shape at batch 2 and 4 runs 14.4 and 14.6 us per step in
+// clusters of up to 16 against 15.3 and 16.2 in clusters of up to 8; one
+// sequence and the 2400-slot ragged batches unchanged). Where clusters of
+// that size cannot be placed the plan falls back to 8.
+constexpr int kDefaultClusterChunks = 16;
+constexpr int kPortableClusterChunks = 8;
 
 // Split the slot axis of every unit into nchunk chunks of chunk_tiles tiles.
 // Each CTA costs a fixed start-up and merge, so chunks stay long (13 to 32
@@ -253,7 +263,7 @@ constexpr int kSplitMinSlots = 8192;
 // beat 3 of 13 on the 2400-slot ragged batch); a batch too small to fill
 // the GPU that way uses short chunks of about 5 tiles instead. At most
 // kMaxChunkTiles tiles and kMaxNChunk chunks.
-Plan plan_split(int S, int units, int sms, bool want_cluster) {
+Plan plan_split(int S, int units, int sms, bool want_cluster, int D, int G, bool score) {
     Plan pl;
     pl.tiles = (S + lf::kTile - 1) / lf::kTile;
     int nchunk = 0;
@@ -275,35 +285,53 @@ Plan plan_split(int S, int units, int sms, bool want_cluster) {
     pl.nchunk = (pl.tiles + pl.chunk_tiles - 1) / pl.chunk_tiles;
     pl.stages = 2;
     if (const char* env = std::getenv("LF_STAGES")) pl.stages = (std::atoi(env) == 3) ? 3 : 2;
-    // A grid that fits in one wave (3 CTAs per SM) of units of at most
-    // kMaxClusterChunks chunks merges inside thread-block clusters: the
+    // A grid whose clusters (one per unit, of at most cmax chunks) are all
+    // resident at once merges inside thread-block clusters: the
     // latency-bound small batches gain the shorter merge. Larger grids keep
     // the last-CTA merge, where a finished CTA frees its slot at once instead
     // of waiting for its cluster. LF_CLUSTER=0 turns clusters off, =1 forces
-    // them whenever the shape allows.
+    // them whenever the shape allows. A cluster must sit within one GPC, so
+    // how many fit at once comes from the occupancy query, not the SM count
+    // (measured: 16 clusters of 8 one-per-SM CTAs, 128 of 152 SMs, took two
+    // waves: 21.6 us per step against 10.4 for one cluster).
     pl.cluster = false;
     const char* cenv = std::getenv("LF_CLUSTER");
     const int cmode = cenv ? std::atoi(cenv) : -1;
-    const bool one_wave = static_cast<long>(units) *
-                              std::min(pl.nchunk, lf::kMaxClusterChunks) <= 3L * sms;
-    if (want_cluster && pl.stages == 2 && cmode != 0 && (cmode == 1 || one_wave) &&
-        pl.tiles <= lf::kMaxClusterChunks * lf::kMaxChunkTiles) {
-        if (pl.nchunk > lf::kMaxClusterChunks) {
-            pl.chunk_tiles = (pl.tiles + lf::kMaxClusterChunks - 1) / lf::kMaxClusterChunks;
-            pl.nchunk = (pl.tiles + pl.chunk_tiles - 1) / pl.chunk_tiles;
+    int cmax = kDefaultClusterChunks;
+    if (const char* env = std::getenv("LF_CLUSTER_MAX"))
+        cmax = std::min(std::max(std::atoi(env), 2), lf::kMaxClusterChunks);
+    const char* denv = std::getenv("LF_DEEP");
+    const int dmode = denv ? std::atoi(denv) : -1;
+    pl.fit = -1;
+    bool first = true;
+    for (int cap : {cmax, std::min(cmax, kPortableClusterChunks)}) {
+        if (!want_cluster || pl.stages != 2 || cmode == 0 || pl.tiles > cap * lf::kMaxChunkTiles)
+            break;
+        int ct = pl.chunk_tiles, nc = pl.nchunk;
+        if (nc > cap) {
+            ct = (pl.tiles + cap - 1) / cap;
+            nc = (pl.tiles + ct - 1) / ct;
         }
-        pl.cluster = true;
-        // A grid of at most one CTA per SM has room for a deep TMA ring: every
-        // tile of a short chunk is in flight at once, which shortens the
-        // chain of round trips of a latency-bound step. It pays from 5 tiles
-        // per chunk (3 turns of a 2-stage ring; measured: one 2400-slot
-        // sequence 12.5 -> 11.5 us per step, a 4-tile chunk no gain).
-        // LF_DEEP=0: off; LF_DEEP=1: also for shorter chunks.
-        const char* denv = std::getenv("LF_DEEP");
-        const int dmode = denv ? std::atoi(denv) : -1;
-        if (dmode != 0 && static_cast<long>(units) * pl.nchunk <= static_cast<long>(sms) &&
-            (dmode == 1 || pl.chunk_tiles >= 5))
-            pl.stages = lf::kDeepStages;
+        const int fit = lf::max_active_clusters(D, G, 2, score, nc);
+        if (first) pl.fit = fit;
+        first = false;
+        if (fit == 0 && nc > kPortableClusterChunks) continue;  // this size cannot be placed
+        if (fit > 0 && (cmode == 1 || units <= fit)) {
+            pl.chunk_tiles = ct;
+            pl.nchunk = nc;
+            pl.cluster = true;
+            // Clusters of one CTA per SM, all resident at once, have room
+            // for a deep TMA ring: every tile of a short chunk is in flight
+            // at once, which shortens the chain of round trips of a
+            // latency-bound step. It pays from 5 tiles per chunk (3 turns of
+            // a 2-stage ring; measured: one 2400-slot sequence 12.5 -> 11.5
+            // us per step, a 4-tile chunk no gain). LF_DEEP=0: off;
+            // LF_DEEP=1: also for shorter chunks.
+            if (dmode != 0 && (dmode == 1 || ct >= 5) &&
+                units <= lf::max_active_clusters(D, G, lf::kDeepStages, score, nc))
+                pl.stages = lf::kDeepStages;
+        }
+        break;
     }
     // Top-1 steps over long units without clusters score in a second kernel:
     // the last CTA's scan of every slot would otherwise run on the step's
@@ -478,7 +506,8 @@ lf_status run_step(const StepArgs& a, const Shape& s, void* stream_v) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    const Plan pl = plan_split(s.S, s.B * s.Hkv, sm_count(dev), a.topk == 1);
+    const Plan pl = plan_split(s.S, s.B * s.Hkv, sm_count(dev), a.topk == 1, s.d, s.Hq / s.Hkv,
+                               a.score);
     const Layout L = scratch_layout(s, pl, 0);
     Scratch* scr = nullptr;
     if ((st = get_scratch(dev, stream, L.total, static_cast<size_t>(s.B) * s.Hkv, &scr)) != LF_OK) return st;
@@ -582,7 +611,7 @@ lf_status lf_decode_step_host(const void* q_host, void* k_cache, void* v_cache, 
     size_t off_q = 0, off_k = align_up(off_q + q_bytes, 256), off_v = align_up(off_k + kv_bytes, 256),
            off_w = align_up(off_v + kv_bytes, 256), off_o = align_up(off_w + i_bytes, 256),
            off_n = align_up(off_o + q_bytes, 256), staging = align_up(off_n + i_bytes, 256);
-    const Plan pl = plan_split(S, static_cast<int>(units), sm_count(dev), true);
+    const Plan pl = plan_split(S, static_cast<int>(units), sm_count(dev), true, d, Hq / Hkv, true);
     const Layout L = scratch_layout(s, pl, staging);
     Scratch* scr = nullptr;
     if ((st = get_scratch(dev, stream, L.total, static_cast<size_t>(s.B) * s.Hkv, &scr)) != LF_OK) return st;
@@ -643,7 +672,7 @@ lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, in
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return cuda_fail(e, "cudaDeviceGetAttribute");
     const size_t units = static_cast<size_t>(B) * Hkv;
-    const Plan pl = plan_split(S, static_cast<int>(units), sms > 0 ? sms : 1, true);
+    const Plan pl = plan_split(S, static_cast<int>(units), sms > 0 ? sms : 1, true, d, Hq / Hkv, true);
     const Layout L = scratch_layout(s, pl, 0);
     const size_t arrivals_off = align_up(L.total, 256);
     const size_t err_off = align_up(arrivals_off + units * sizeof(uint32_t), 256);
@@ -695,10 +724,30 @@ lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, in
                                static_cast<int>(units), stream);
     if (e != cudaSuccess && pl.cluster) {
         (void)cudaGetLastError();
-        e = lf::launch_decode_step(d, g, pl.stages, true, false, tmK, tmV, sp,
-                                   static_cast<int>(units), stream);
+        e = lf::launch_decode_step(d, g, 2, true, false, tmK, tmV, sp, static_cast<int>(units),
+                                   stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");
+    return LF_OK;
+}
+
+lf_status lf_step_plan(int B, int Hq, int Hkv, int d, int S, int topk, int32_t* plan) {
+    if (!plan) return fail(LF_ERR_INVALID_ARG, "plan is null");
+    if (topk < 1 || topk > LF_MAX_TOPK)
+        return fail(LF_ERR_INVALID_ARG, "k = %d is outside [1, %d]", topk, LF_MAX_TOPK);
+    const Shape s{B, Hq, Hkv, d, S, 0, 1.f};
+    lf_status st = check_shape(s);
+    if (st != LF_OK) return st;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const Plan pl = plan_split(S, B * Hkv, sm_count(dev), topk == 1, d, Hq / Hkv, true);
+    plan[0] = pl.nchunk;
+    plan[1] = pl.chunk_tiles;
+    plan[2] = pl.stages;
+    plan[3] = pl.cluster ? 1 : 0;
+    plan[4] = pl.split ? 1 : 0;
+    plan[5] = pl.fit;
     return LF_OK;
 }
 

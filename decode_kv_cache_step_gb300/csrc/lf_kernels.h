@@ -54,7 +54,8 @@ struct StepParams {
 constexpr int kFlagFillEmptyFirst = 1;  // empty (masked) slots are returned before any score
 constexpr int kFlagMaskEvicted = 2;     // returned slots are masked (-1) in place
 constexpr int kMaxTopK = 1024;
-constexpr int kMaxClusterChunks = 8;    // chunks of a unit run as one cluster up to this
+constexpr int kMaxClusterChunks = 16;   // chunks of a unit run as one cluster up to this
+                                        // (above 8: a non-portable cluster size)
 constexpr int kDeepStages = 6;          // TMA ring of the one-CTA-per-SM cluster variant
 
 // Dynamic shared memory the kernel needs for head dim D and a TMA ring of
@@ -80,6 +81,11 @@ cudaError_t launch_decode_step_cluster(int D, int G, int stages, bool score,
                                        const CUtensorMap& tmK, const CUtensorMap& tmV,
                                        const StepParams& p, int units, cudaStream_t stream,
                                        bool pdl);
+
+// How many clusters of csize CTAs (one unit each) of the cluster instance
+// (stages 2 or kDeepStages) can be resident at once on the current device;
+// 0 if none can or the query fails. Cached per device and instance.
+int max_active_clusters(int D, int G, int stages, bool score, int csize);
 
 // The scoring kernel of a split finish: grid (nchunk, units); CTA (c, u)
 // scores chunk c of unit u from the ages, the score terms and c_h, and the

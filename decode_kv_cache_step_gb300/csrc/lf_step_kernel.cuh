@@ -762,11 +762,17 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
     const int nchunk = p.nchunk;
     const uint32_t rank = cluster_ctarank();
     constexpr int kWBytes = (kConsumerWarps * G * D + 2 * kConsumerWarps * G) * 4;
+    // The arrays below overlay the TMA ring, which the main loop has drained.
+    static_assert(((kWBytes + 15) & ~15) +
+                          (G * D + 2 * G + 2 * kMaxClusterChunks + 3 * kMaxClusterChunks * G +
+                           2 * G + 2 * kConsumerWarps) * 4 <=
+                      StepSmem<D, kStages>::kAgesOff,
+                  "cluster epilogue arrays exceed the TMA ring");
     float* pub_o = reinterpret_cast<float*>(smem + ((kWBytes + 15) & ~15));  // [G][D]
     float2* pub_ml = reinterpret_cast<float2*>(pub_o + G * D);               // [G]
     // Every CTA's local best, written into rank 0's copy of these arrays.
-    float* pub_best = reinterpret_cast<float*>(pub_ml + G);                  // [8]
-    int* pub_bestj = reinterpret_cast<int*>(pub_best + kMaxClusterChunks);   // [8]
+    float* pub_best = reinterpret_cast<float*>(pub_ml + G);                  // [16]
+    int* pub_bestj = reinterpret_cast<int*>(pub_best + kMaxClusterChunks);   // [16]
     float2* s_mlc = reinterpret_cast<float2*>(pub_bestj + kMaxClusterChunks);  // [nchunk][G]
     float* s_w = reinterpret_cast<float*>(s_mlc + kMaxClusterChunks * G);    // [nchunk][G]
     float* s_m = s_w + kMaxClusterChunks * G;                               // [G]
@@ -1379,12 +1385,11 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
                               reinterpret_cast<uint64_t*>(smem + L::kScanBarOff), tid);
 }
 
+// Sets the kernel's function attributes (shared memory above 48 KB; cluster
+// instances: clusters of more than 8 CTAs, an opt-in size) once per device.
 template <int D, int G, int kStages, bool kScore, bool kCluster>
-cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
-                     int units, cudaStream_t stream, bool pdl) {
+cudaError_t configure_t() {
     using L = StepSmem<D, kStages>;
-    if (finish_smem_bytes(p.nchunk, G, kScore ? p.topk : 1) > static_cast<size_t>(L::kBarOff))
-        return cudaErrorInvalidConfiguration;
     auto kernel = lf_decode_step_kernel<D, G, kStages, kScore, kCluster>;
     static int configured_for = -1;
     int dev = 0;
@@ -1393,8 +1398,49 @@ cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepP
     if (configured_for != dev) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
         if (e != cudaSuccess) return e;
+        if constexpr (kCluster) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
         configured_for = dev;
     }
+    return cudaSuccess;
+}
+
+// How many clusters of `csize` CTAs of the cluster instance can be resident
+// at once on the current device (0: none, or the query failed).
+template <int D, int G, int kStages, bool kScore>
+int max_active_clusters_t(int csize) {
+    if (configure_t<D, G, kStages, kScore, true>() != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(csize, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = StepSmem<D, kStages>::kAlloc;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = static_cast<unsigned>(csize);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, lf_decode_step_kernel<D, G, kStages, kScore, true>,
+                                       &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int D, int G, int kStages, bool kScore, bool kCluster>
+cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
+                     int units, cudaStream_t stream, bool pdl) {
+    using L = StepSmem<D, kStages>;
+    if (finish_smem_bytes(p.nchunk, G, kScore ? p.topk : 1) > static_cast<size_t>(L::kBarOff))
+        return cudaErrorInvalidConfiguration;
+    auto kernel = lf_decode_step_kernel<D, G, kStages, kScore, kCluster>;
+    cudaError_t e = configure_t<D, G, kStages, kScore, kCluster>();
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.nchunk, units);
     cfg.blockDim = dim3(kThreads);

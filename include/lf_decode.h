@@ -57,6 +57,8 @@
  *   LF_CHUNK_TILES=n   64-slot tiles per chunk of the slot axis (1..32)
  *   LF_STAGES=3        three-stage TMA ring (two CTAs per SM) instead of two
  *   LF_CLUSTER=0|1     thread-block-cluster merge off / on wherever it fits
+ *   LF_CLUSTER_MAX=n   largest cluster, 2..16 CTAs (default 16, a
+ *                      non-portable size; 8 where 16 cannot be placed)
  *   LF_DEEP=0|1        cluster grids of at most one CTA per SM keep the
  *                      2-stage TMA ring / take the deep one even for chunks
  *                      of fewer than 5 tiles
@@ -236,6 +238,22 @@ lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, in
  * stream has never run a step.
  */
 lf_status lf_device_errors(void* stream, uint32_t* flags, int clear);
+
+/*
+ * The launch plan lf_decode_step / lf_decode_step_ex (k = topk, score on)
+ * take for this shape on the current device under the present LF_*
+ * environment switches. Launches nothing; queries the device's SM count and
+ * cluster occupancy (and sets the kernels' function attributes) on first use.
+ * plan (host, 6 entries, written on LF_OK):
+ *   [0] chunks per unit (CTAs per unit)   [1] 64-slot tiles per chunk
+ *   [2] TMA ring stages                   [3] 1: a unit's chunks run as one
+ *                                             thread-block cluster
+ *   [4] 1: split finish (scoring kernel)  [5] clusters of the largest size
+ *       tried that can be resident at once (-1: clusters not considered)
+ * Errors: LF_ERR_INVALID_ARG / LF_ERR_UNSUPPORTED as for a step of this
+ * shape; LF_ERR_CUDA without a usable device.
+ */
+lf_status lf_step_plan(int B, int Hq, int Hkv, int d, int S, int topk, int32_t* plan);
 
 /*
  * Kernel timing. While enabled, every kernel launch of the library is

@@ -160,18 +160,42 @@ def test_split_shapes_do_not_change_results(monkeypatch, chunk_tiles, cluster, s
 @pytest.mark.parametrize("name", ["qwen3_8b_b1_s2400", "tiny_b2_s256"])
 def test_two_stage_cluster_path_every_step(monkeypatch, name):
     """The cluster merge with the 2-stage TMA ring (grids of more than one CTA
-    per SM; the small workloads take the deep ring by default)."""
+    per SM, or chunks of fewer than 5 tiles), with the deep ring off."""
     monkeypatch.setenv("LF_DEEP", "0")
     wl = WORKLOADS[name]
     run_parity(wl, min(wl.steps, 32))
 
 
+@pytest.mark.parametrize("deep", ["0", "1"])
+@pytest.mark.parametrize("cmax", ["5", "8", "16"])
+def test_cluster_sizes_every_step(monkeypatch, cmax, deep):
+    """Clusters capped at 5 CTAs (an odd split of the output row among the
+    CTAs), 8 (the portable size; chunks of 5 tiles) and 16 (the default, a
+    non-portable size; chunks of 3 tiles), in the deep and the 2-stage TMA
+    ring."""
+    monkeypatch.setenv("LF_CLUSTER_MAX", cmax)
+    monkeypatch.setenv("LF_DEEP", deep)
+    wl = WORKLOADS["qwen3_8b_b1_s2400"]
+    run_parity(wl, min(wl.steps, 32))
+
+
+@pytest.mark.parametrize("cmax", ["12", "16"])
+def test_cluster_sizes_long_units(monkeypatch, cmax):
+    """16K-slot units forced into clusters of 12 or 16 CTAs (chunks of 22 or
+    16 tiles)."""
+    monkeypatch.setenv("LF_CLUSTER", "1")
+    monkeypatch.setenv("LF_CLUSTER_MAX", cmax)
+    wl = WORKLOADS["long_b32_s16384_ragged"].with_batch(2)
+    run_parity(wl, steps=2)
+
+
 @pytest.mark.parametrize("split", ["0", "1"])
 @pytest.mark.parametrize("name", ["qwen3_8b_b1_s2400", "tiny_b2_s256"])
 def test_last_cta_merge_path_every_step(monkeypatch, name, split):
-    """The merge by the unit's last CTA (used when clusters are off or a unit
-    has more than 8 chunks) on every step of the small workloads, scoring in
-    the same kernel or in the split-finish kernel."""
+    """The merge by the unit's last CTA (used when clusters are off, a unit
+    has more chunks than a cluster holds or the clusters would not all be
+    resident at once) on every step of the small workloads, scoring in the
+    same kernel or in the split-finish kernel."""
     monkeypatch.setenv("LF_CLUSTER", "0")
     monkeypatch.setenv("LF_SPLIT", split)
     wl = WORKLOADS[name]

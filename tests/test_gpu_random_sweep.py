@@ -1,8 +1,8 @@
 """Seeded random sweep against the fp64 oracle: shapes (d, g, heads, batch,
 S from 1 to 9000), masks (random or ragged prefixes), windows, write modes,
 entry points and selection options, each under a random launch plan
-(clusters on or off, split finish on or off, forced chunk sizes, deep or
-2-stage cluster ring). The comparison rules are the parity suite's."""
+(clusters on or off and of up to 16 CTAs, split finish on or off, forced
+chunk sizes, deep or 2-stage cluster ring). The comparison rules are the parity suite's."""
 import numpy as np
 import pytest
 import torch
@@ -43,6 +43,9 @@ def _draw(i):
             env[name] = c
     if rng.random() < 0.4:
         env["LF_CHUNK_TILES"] = str(int(rng.integers(1, 33)))
+    crng = np.random.default_rng(9000 + i)  # a stream of its own: the draws above stay
+    if crng.random() < 0.3:
+        env["LF_CLUSTER_MAX"] = str(int(crng.integers(2, 17)))
     entry = str(rng.choice(["step", "scores", "ex"]))
     k = int(rng.choice([1, 2, 17]))
     flags = int(rng.integers(0, 4))

@@ -240,8 +240,8 @@ struct Plan {
     int tiles, chunk_tiles, nchunk, stages;
     bool cluster;  // the unit's chunks run as one thread-block cluster
     bool split;    // a top-1 step scores in a second kernel (split finish)
-    int fit = 0;   // clusters of the first size tried that can be resident at once
-                   // (-1: clusters not considered)
+    int fit = 0;   // clusters that can be resident at once: of the plan's size with a
+                   // cluster merge, else of the largest size tried (-1: not considered)
 };
 
 // Units of at least this many slots take the split finish.
@@ -312,14 +312,37 @@ Plan plan_split(int S, int units, int sms, bool want_cluster, int D, int G, bool
             ct = (pl.tiles + cap - 1) / cap;
             nc = (pl.tiles + ct - 1) / ct;
         }
-        const int fit = lf::max_active_clusters(D, G, 2, score, nc);
+        int fit = lf::max_active_clusters(D, G, 2, score, nc);
         if (first) pl.fit = fit;
         first = false;
         if (fit == 0 && nc > kPortableClusterChunks) continue;  // this size cannot be placed
+        if (fit > 0 && units > fit && cmode != 1) {
+            // Too many units for clusters of nc: take the largest smaller
+            // cluster (longer chunks, at most kMaxChunkTiles tiles) whose
+            // clusters are all resident at once. Measured against the
+            // last-CTA plan: the 3200-slot Qwen3 shape at batch 8, 6 chunks of
+            // 9 tiles in clusters 22.1 us per step against 29.9 for 10 of 5;
+            // at batch 16, 3 of 17 in clusters 40.5 against 50.1 for 4 of 13;
+            // four 16K-slot sequences, 10 of 26 in clusters 44.1 against 58.7
+            // for 20 of 13 with the split finish.
+            for (int n2 = nc - 1; n2 >= 1; --n2) {
+                const int ct2 = (pl.tiles + n2 - 1) / n2;
+                if (ct2 > lf::kMaxChunkTiles) break;
+                const int nc2 = (pl.tiles + ct2 - 1) / ct2;
+                const int f2 = lf::max_active_clusters(D, G, 2, score, nc2);
+                if (units <= f2) {
+                    ct = ct2;
+                    nc = nc2;
+                    fit = f2;
+                    break;
+                }
+            }
+        }
         if (fit > 0 && (cmode == 1 || units <= fit)) {
             pl.chunk_tiles = ct;
             pl.nchunk = nc;
             pl.cluster = true;
+            pl.fit = fit;
             // Clusters of one CTA per SM, all resident at once, have room
             // for a deep TMA ring: every tile of a short chunk is in flight
             // at once, which shortens the chain of round trips of a

@@ -248,8 +248,9 @@ lf_status lf_device_errors(void* stream, uint32_t* flags, int clear);
  *   [0] chunks per unit (CTAs per unit)   [1] 64-slot tiles per chunk
  *   [2] TMA ring stages                   [3] 1: a unit's chunks run as one
  *                                             thread-block cluster
- *   [4] 1: split finish (scoring kernel)  [5] clusters of the largest size
- *       tried that can be resident at once (-1: clusters not considered)
+ *   [4] 1: split finish (scoring kernel)  [5] how many clusters of the
+ *       plan's size can be resident at once (without a cluster merge: of
+ *       the largest size tried; -1: clusters not considered)
  * Errors: LF_ERR_INVALID_ARG / LF_ERR_UNSUPPORTED as for a step of this
  * shape; LF_ERR_CUDA without a usable device.
  */

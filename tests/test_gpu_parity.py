@@ -189,6 +189,18 @@ def test_cluster_sizes_long_units(monkeypatch, cmax):
     run_parity(wl, steps=2)
 
 
+@pytest.mark.parametrize("name,batch", [("qwen3_8b_b128_s3200", 8), ("qwen3_8b_b128_s3200", 16),
+                                        ("long_b32_s16384_ragged", 4)])
+def test_mid_batch_cluster_plans(name, batch):
+    """Mid-size batches whose default plan takes longer chunks so that every
+    unit's cluster is resident at once (6 chunks of 9 tiles, 3 of 17, 12 of
+    22 on GB300)."""
+    wl = WORKLOADS[name].with_batch(batch)
+    p = lf.step_plan(wl.B, wl.Hq, wl.Hkv, wl.d, wl.S)
+    assert p["cluster"] and wl.units <= p["cluster_fit"], p
+    run_parity(wl, steps=3, sample=_sample_units(wl, 14, seed=batch))
+
+
 @pytest.mark.parametrize("split", ["0", "1"])
 @pytest.mark.parametrize("name", ["qwen3_8b_b1_s2400", "tiny_b2_s256"])
 def test_last_cta_merge_path_every_step(monkeypatch, name, split):

@@ -28,16 +28,35 @@ def test_plan_covers_the_slots(shape):
         assert p["cluster"]
 
 
+@pytest.mark.parametrize("cmax", [None, "8", "4"])
 @pytest.mark.parametrize("shape", SHAPES)
-def test_clusters_only_when_all_resident(monkeypatch, shape):
+def test_clusters_only_when_all_resident(monkeypatch, shape, cmax):
     """Without LF_CLUSTER=1 a cluster plan has every unit's cluster resident
-    at once (the largest size tried, or the portable 8 when that size cannot
-    be placed at all)."""
+    at once, within the cap."""
     B, Hq, Hkv, d, S = shape
-    monkeypatch.setenv("LF_CLUSTER_MAX", "8")
+    if cmax:
+        monkeypatch.setenv("LF_CLUSTER_MAX", cmax)
     p = lf.step_plan(B, Hq, Hkv, d, S)
     if p["cluster"]:
-        assert p["nchunk"] <= 8 and B * Hkv <= p["cluster_fit"]
+        assert p["nchunk"] <= int(cmax or 16) and B * Hkv <= p["cluster_fit"]
+
+
+@pytest.mark.parametrize("B,S", [(8, 3200), (16, 3200), (20, 2400), (4, 16384), (2, 30000)])
+def test_longer_chunks_to_fit_clusters(monkeypatch, B, S):
+    """A batch too large for clusters of its short-chunk plan takes fewer,
+    longer chunks whose clusters all fit; the next larger cluster would not."""
+    Hq, Hkv, d = 32, 8, 128
+    p = lf.step_plan(B, Hq, Hkv, d, S)
+    assert p["cluster"] and B * Hkv <= p["cluster_fit"], p
+    tiles = -(-S // TILE)
+    ct_next = -(-tiles // (p["nchunk"] + 1))
+    if p["nchunk"] < 16 and ct_next < p["chunk_tiles"]:
+        # Forced clusters of the next size report how many fit at once.
+        monkeypatch.setenv("LF_CHUNK_TILES", str(ct_next))
+        monkeypatch.setenv("LF_CLUSTER", "1")
+        q = lf.step_plan(B, Hq, Hkv, d, S)
+        assert q["cluster"] and q["nchunk"] > p["nchunk"], (p, q)
+        assert B * Hkv > q["cluster_fit"], (p, q)
 
 
 @pytest.mark.parametrize("shape", SHAPES)

@@ -260,9 +260,12 @@ constexpr int kPortableClusterChunks = 8;
 // tiles) while the grid still has about 27 CTAs per SM (about 4100), the
 // chunk count rounded down, to balance the tail (measured: 4 chunks of 13
 // tiles beat 3 of 17 on the Fig. 1 shape by 1 us per step, 2 chunks of 19
-// beat 3 of 13 on the 2400-slot ragged batch); a batch too small to fill
-// the GPU that way uses short chunks of about 5 tiles instead. At most
-// kMaxChunkTiles tiles and kMaxNChunk chunks.
+// beat 3 of 13 on the 2400-slot ragged batch); units long enough for the
+// split finish, which has no last-CTA scan on the tail, aim at 16 tiles
+// (measured on 8 sequences of 16K slots: 16 chunks of 16 tiles 75.6 us per
+// step against 80.5 for 20 of 13). A batch too small to fill the GPU that
+// way uses short chunks of about 5 tiles instead. At most kMaxChunkTiles
+// tiles and kMaxNChunk chunks.
 Plan plan_split(int S, int units, int sms, bool want_cluster, int D, int G, bool score) {
     Plan pl;
     pl.tiles = (S + lf::kTile - 1) / lf::kTile;
@@ -271,11 +274,13 @@ Plan plan_split(int S, int units, int sms, bool want_cluster, int D, int G, bool
         const int ct = std::atoi(env);
         if (ct >= 1 && ct <= lf::kMaxChunkTiles) nchunk = (pl.tiles + ct - 1) / ct;
     }
+    const bool forced_chunks = nchunk > 0;
     if (nchunk == 0) {
         const int longest = (pl.tiles + lf::kMaxChunkTiles - 1) / lf::kMaxChunkTiles;
         const int fill = static_cast<int>((27L * sms) / units);
+        const int target = S >= kSplitMinSlots ? 16 : 13;
         if (static_cast<long>(units) * longest >= sms)
-            nchunk = std::max(longest, std::min(fill, (pl.tiles + 12) / 13));
+            nchunk = std::max(longest, std::min(fill, (pl.tiles + target - 1) / target));
         else
             nchunk = (pl.tiles + 4) / 5;
     }
@@ -316,7 +321,7 @@ Plan plan_split(int S, int units, int sms, bool want_cluster, int D, int G, bool
         if (first) pl.fit = fit;
         first = false;
         if (fit == 0 && nc > kPortableClusterChunks) continue;  // this size cannot be placed
-        if (fit > 0 && units > fit && cmode != 1) {
+        if (fit > 0 && units > fit && cmode != 1 && !forced_chunks) {
             // Too many units for clusters of nc: take the largest smaller
             // cluster (longer chunks, at most kMaxChunkTiles tiles) whose
             // clusters are all resident at once. Measured against the

@@ -54,7 +54,8 @@
  * Environment switches, read at every call (tuning and tests; every setting
  * stays within the same tolerances of the exact result, and LF_SPLIT,
  * LF_SCORE_PARTS and LF_PDL change no result bit):
- *   LF_CHUNK_TILES=n   64-slot tiles per chunk of the slot axis (1..32)
+ *   LF_CHUNK_TILES=n   64-slot tiles per chunk of the slot axis (1..32);
+ *                      a cluster merge may still re-chunk to its size cap
  *   LF_STAGES=3        three-stage TMA ring (two CTAs per SM) instead of two
  *   LF_CLUSTER=0|1     thread-block-cluster merge off / on wherever it fits
  *   LF_CLUSTER_MAX=n   largest cluster, 2..16 CTAs (default 16, a

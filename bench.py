@@ -262,12 +262,32 @@ def bench_reference(args, wl):
     return 0
 
 
-def workload_config(wl, world, layers=1):
-    return {"workload": wl.name, "layers": layers, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d, "S": wl.S,
-            "W": wl.W, "live": list(wl.live) if isinstance(wl.live, tuple) else wl.live,
-            "description": wl.description,
-            "l2": "inputs larger than L2 (K/V caches >> 129 MB); no flush between steps",
-            "parallelism": f"replicas x{world} (disjoint sequences, no collective)"}
+L2_BYTES = 129 * 2**20
+
+
+def l2_note(wl, layers=1) -> str:
+    """How the timed steps relate to L2 (no flush between steps in any case)."""
+    kv = wl.B * wl.Hkv * wl.S * wl.d * 2 * 2
+    if kv > L2_BYTES:
+        return f"inputs larger than L2 (K/V caches {kv / 2**20:.0f} MiB > 129 MiB); no flush between steps"
+    if kv * layers > L2_BYTES:
+        return (f"{layers} caches of {kv / 2**20:.1f} MiB stepped in turn "
+                f"({kv * layers / 2**20:.0f} MiB > 129 MiB L2); no flush between steps")
+    need = L2_BYTES // kv + 1
+    return (f"inputs fit in L2 (K/V caches {kv / 2**20:.2f} MiB) and stay resident between "
+            f"steps (no flush); --layers {need} or more steps that many caches in turn so that "
+            "each step reads DRAM")
+
+
+def workload_config(wl, world, layers=1, plan=None):
+    cfg = {"workload": wl.name, "layers": layers, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+           "S": wl.S, "W": wl.W, "live": list(wl.live) if isinstance(wl.live, tuple) else wl.live,
+           "description": wl.description,
+           "l2": l2_note(wl, layers),
+           "parallelism": f"replicas x{world} (disjoint sequences, no collective)"}
+    if plan is not None:
+        cfg["launch_plan"] = plan
+    return cfg
 
 
 def bench_lf(args, wl):
@@ -524,7 +544,8 @@ def bench_lf(args, wl):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": workload_config(wl, world, L),
+        "config": workload_config(wl, world, L,
+                                  plan=lf.step_plan(wl.B, wl.Hq, wl.Hkv, wl.d, wl.S)),
         "hbm": {"algorithmic_bytes_per_step": alg, "achieved_gbs": step_gbs,
                 "frac_of_measured_peak": step_gbs / peak, "frac_of_8000_gbs": step_gbs / 8000.0,
                 "peak_kind": peak_kind},

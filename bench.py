@@ -483,23 +483,47 @@ def bench_lf(args, wl):
     h_slots = [[torch.full((wl.B, wl.Hkv), -1, dtype=torch.int32).pin_memory(),
                 torch.empty((wl.B, wl.Hkv), dtype=torch.int32).pin_memory()] for _ in range(L)]
 
+    # The serving loop's call: one prepared step per layer, input set and
+    # slot parity (lf_step_prepare once; each step is one lf_step_run).
+    handles = [[lf.PreparedStep(hpool[j]["q"], kk, vv, mm, hpool[j]["new_k"], hpool[j]["new_v"],
+                                h_slots[li][j % 2], h_out, h_slots[li][(j + 1) % 2], wl.W,
+                                wl.scale, stream=stream)
+                for j in range(len(hpool))] for li, (kk, vv, mm) in enumerate(layers)]
+
     def e2e_step(i):
+        for hl in handles:
+            hl[i % len(hpool)].run()
+        stream.synchronize()
+
+    # The per-call entry point (argument checks, plan and pointer queries
+    # every call), for comparison.
+    def e2e_step_unprepared(i):
         p = hpool[i % len(hpool)]
         for li, (kk, vv, mm) in enumerate(layers):
             lf.decode_step_host(p["q"], kk, vv, mm, p["new_k"], p["new_v"], h_slots[li][i % 2],
                                 h_out, h_slots[li][(i + 1) % 2], wl.W, wl.scale, stream=stream)
         stream.synchronize()
 
-    n_e2e_warm = min(args.warmup, 6)
-    for i in range(n_e2e_warm):
-        e2e_step(i)
-    if world > 1:
-        torch.distributed.barrier()
-    t0 = time.perf_counter()
-    for i in range(n_e2e_warm, n_e2e_warm + args.steps):
-        e2e_step(i)
-    e2e_s = time.perf_counter() - t0
-    e2e_s = max_over_ranks(e2e_s, device)
+    def timed(fn, i0):
+        n_warm = min(args.warmup, 6)
+        for i in range(i0, i0 + n_warm):
+            fn(i)
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for i in range(i0 + n_warm, i0 + n_warm + args.steps):
+            fn(i)
+        return max_over_ranks(time.perf_counter() - t0, device), i0 + n_warm + args.steps
+
+    # Both loops continue the same token sequence (even step counts keep the
+    # slot parity of each loop's first step).
+    e2e_s, i_next = timed(e2e_step, 0)
+    e2e_plain_s, _ = timed(e2e_step_unprepared, i_next + (i_next % 2))
+    if lf.device_errors(stream) != 0 or any(h.errors() for hl in handles for h in hl):
+        raise RuntimeError("device error word set during the end-to-end steps")
+    for hl in handles:
+        for h in hl:
+            h.close()
     clocks.stop()
     h2d = L * ((wl.B * wl.Hq * wl.d * 2) + 2 * (wl.B * wl.Hkv * wl.d * 2) + wl.B * wl.Hkv * 4)
     d2h = L * (wl.B * wl.Hq * wl.d * 2 + wl.B * wl.Hkv * 4)
@@ -567,10 +591,14 @@ def bench_lf(args, wl):
         "cpu_baseline": cpu,
         "e2e": {"value": world * args.steps / e2e_s, "unit": "steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "lf_decode_step_host per layer from pinned host buffers (the kernel "
-                       "reads inputs and writes results in host memory in place over the "
-                       "host link; LF_HOST_ZEROCOPY=0 stages them with copies); stream sync "
-                       "every step"},
+                "how": "PreparedStep.run (lf_step_run) per layer on pinned host buffers: the "
+                       "kernel reads the step's inputs and writes its results in host memory "
+                       "in place over the host link (LF_HOST_ZEROCOPY=0 stages them with "
+                       "copies); stream sync every step, the next slot read back from host "
+                       "memory as the next step's write slot",
+                "per_call_entry_value": world * args.steps / e2e_plain_s,
+                "per_call_entry": "lf_decode_step_host per layer (checks, plan and pointer "
+                                  "queries every call), same buffers"},
         "gpu_launches": args.steps * L * launches_per_layer,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }

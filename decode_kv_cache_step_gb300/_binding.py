@@ -39,7 +39,8 @@ LF_MAX_TOPK = 1024
 # Every exported symbol of include/lf_decode.h.
 EXPORTED = (
     "lf_decode_step", "lf_decode_step_scores", "lf_decode_step_ex", "lf_decode_attention",
-    "lf_decode_step_host", "lf_decode_step_noalloc", "lf_step_plan", "lf_device_errors",
+    "lf_decode_step_host", "lf_decode_step_noalloc", "lf_step_prepare", "lf_step_run",
+    "lf_step_errors", "lf_step_destroy", "lf_step_plan", "lf_device_errors",
     "lf_profile_enable", "lf_profile_collect", "lf_release_workspace", "lf_status_string",
     "lf_last_error", "lf_version",
 )
@@ -89,6 +90,14 @@ def load_library(path: str | None = None):
         lib.lf_decode_attention.restype = I
         for fn in (lib.lf_decode_step, lib.lf_decode_step_host, lib.lf_decode_step_scores):
             fn.restype = I
+        lib.lf_step_prepare.argtypes = [P] * 9 + [I] * 6 + [F, P, ctypes.POINTER(P)]
+        lib.lf_step_prepare.restype = I
+        lib.lf_step_run.argtypes = [P]
+        lib.lf_step_run.restype = I
+        lib.lf_step_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I]
+        lib.lf_step_errors.restype = I
+        lib.lf_step_destroy.argtypes = [P]
+        lib.lf_step_destroy.restype = I
         lib.lf_step_plan.argtypes = [I] * 6 + [ctypes.POINTER(ctypes.c_int32)]
         lib.lf_step_plan.restype = I
         lib.lf_device_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I]
@@ -256,6 +265,72 @@ def decode_step_noalloc(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), mask.data_ptr(), new_k.data_ptr(),
         new_v.data_ptr(), write_slot.data_ptr(), out.data_ptr(), next_slot.data_ptr(),
         B, Hq, Hkv, d, S, int(W), float(scale), _stream_handle(stream)))
+
+
+class PreparedStep:
+    """lf_step_prepare / lf_step_run: one layer's decode step with its buffers,
+    shape, plan and stream fixed once; ``run()`` then enqueues the step with
+    no argument checks (see include/lf_decode.h). The per-step buffers (q,
+    new_k, new_v, write_slot, out, next_slot) may each be CUDA tensors, pinned
+    host tensors (read and written in place) or other host tensors (staged);
+    the caches and the mask are CUDA tensors. The object keeps the tensors
+    alive; write each token's inputs into the same tensors."""
+
+    def __init__(self, q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slot, W,
+                 scale, stream=None):
+        lib = load_library()
+        B, Hq, Hkv, d, S = _shapes(q, k_cache)
+        bf, i32 = torch.bfloat16, torch.int32
+        _need(k_cache, "k_cache", bf, (B, Hkv, S, d), True)
+        _need(v_cache, "v_cache", bf, (B, Hkv, S, d), True)
+        _need(mask, "mask", i32, (B, Hkv, S), True)
+        for t, name, dt, shape in ((q, "q", bf, (B, Hq, d)), (new_k, "new_k", bf, (B, Hkv, d)),
+                                   (new_v, "new_v", bf, (B, Hkv, d)),
+                                   (write_slot, "write_slot", i32, (B, Hkv)),
+                                   (out, "out", bf, (B, Hq, d)),
+                                   (next_slot, "next_slot", i32, (B, Hkv))):
+            _need(t, name, dt, shape, t.is_cuda if isinstance(t, torch.Tensor) else True)
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        self._keep = (q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slot, stream)
+        self._lib = lib
+        self._h = ctypes.c_void_p(0)
+        _check(lib, lib.lf_step_prepare(
+            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), mask.data_ptr(),
+            new_k.data_ptr(), new_v.data_ptr(), write_slot.data_ptr(), out.data_ptr(),
+            next_slot.data_ptr(), B, Hq, Hkv, d, S, int(W), float(scale),
+            _stream_handle(stream), ctypes.byref(self._h)))
+        self._run = lib.lf_step_run
+
+    def run(self):
+        """Enqueue one step on the prepare-time stream (asynchronous)."""
+        st = self._run(self._h)
+        if st:
+            _check(self._lib, st)
+
+    def errors(self, clear: bool = True) -> int:
+        """OR of LF_DEVERR_* bits of this handle's runs (syncs its stream)."""
+        flags = ctypes.c_uint32(0)
+        _check(self._lib, self._lib.lf_step_errors(self._h, ctypes.byref(flags), int(clear)))
+        return int(flags.value)
+
+    def close(self):
+        """Synchronise the stream and free the handle (idempotent)."""
+        if self._h and self._h.value:
+            h, self._h = self._h, ctypes.c_void_p(0)
+            _check(self._lib, self._lib.lf_step_destroy(h))
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def step_plan(B: int, Hq: int, Hkv: int, d: int, S: int, topk: int = 1) -> dict:

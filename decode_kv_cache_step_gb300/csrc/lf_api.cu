@@ -12,6 +12,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <new>
 #include <utility>
 #include <vector>
 
@@ -453,17 +454,26 @@ Layout scratch_layout(const Shape& s, const Plan& pl, size_t extra) {
 }
 
 // Enqueue one step. Arguments are already checked.
-lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, Scratch* scr,
-                       const Layout& L, const Plan& pl) {
+// Everything one step's launches need, resolved from the arguments, the
+// scratch and the plan.
+struct Launch {
+    lf::StepParams sp;
+    CUtensorMap tmK, tmV;
+    Plan pl;
+    int d, g, units;
+    bool score;
+};
+
+lf_status build_launch(const StepArgs& a, const Shape& s, char* base, uint32_t* arrivals,
+                       uint32_t* dev_err, const Layout& L, const Plan& pl, Launch* out) {
     const int units = s.B * s.Hkv;
     const int g = s.Hq / s.Hkv;
-    CUtensorMap tmK, tmV;
-    lf_status st = encode_cache_map(&tmK, a.k_cache, s.d, s.S, units);
+    Launch& r = *out;
+    lf_status st = encode_cache_map(&r.tmK, a.k_cache, s.d, s.S, units);
     if (st != LF_OK) return st;
-    if ((st = encode_cache_map(&tmV, a.v_cache, s.d, s.S, units)) != LF_OK) return st;
-
-    char* base = static_cast<char*>(scr->base);
-    lf::StepParams sp;
+    if ((st = encode_cache_map(&r.tmV, a.v_cache, s.d, s.S, units)) != LF_OK) return st;
+    lf::StepParams& sp = r.sp;
+    sp = lf::StepParams{};
     sp.q = static_cast<const __nv_bfloat16*>(a.q);
     sp.k_cache = static_cast<__nv_bfloat16*>(a.k_cache);
     sp.v_cache = static_cast<__nv_bfloat16*>(a.v_cache);
@@ -477,12 +487,12 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
     sp.part_o = reinterpret_cast<float*>(base + L.o);
     sp.part_ml = reinterpret_cast<float2*>(base + L.ml);
     sp.stash = reinterpret_cast<float*>(base + L.stash);
-    sp.arrivals = scr->arrivals;
-    sp.dev_err = scr->dev_err;
+    sp.arrivals = arrivals;
+    sp.dev_err = dev_err;
     sp.cfold = reinterpret_cast<float*>(base + L.cfold);
     sp.part_tiles = reinterpret_cast<uint32_t*>(base + L.tiles);
-    sp.score_arrivals = scr->arrivals + units;
-    sp.best = reinterpret_cast<unsigned long long*>(scr->arrivals + 2 * static_cast<size_t>(units));
+    sp.score_arrivals = arrivals + units;
+    sp.best = reinterpret_cast<unsigned long long*>(arrivals + 2 * static_cast<size_t>(units));
     sp.Hq = s.Hq;
     sp.Hkv = s.Hkv;
     sp.S = s.S;
@@ -498,7 +508,15 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
         return fail(LF_ERR_UNSUPPORTED,
                     "k = %d with %d chunks of the slot axis does not fit in shared memory",
                     sp.topk, pl.nchunk);
+    r.pl = pl;
+    r.d = s.d;
+    r.g = g;
+    r.units = units;
+    r.score = a.score;
+    return LF_OK;
+}
 
+lf_status launch(const Launch& r, cudaStream_t stream) {
     // A named range around each launch for timeline profilers (nsys).
     struct NvtxRange {
         explicit NvtxRange(const char* n) { nvtxRangePushA(n); }
@@ -506,25 +524,36 @@ lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, S
     };
     cudaError_t e;
     {
-        NvtxRange range(a.score ? "lf_decode_step" : "lf_decode_attention");
-        ProfScope prof(a.score ? LF_KERNEL_DECODE_STEP : LF_KERNEL_ATTENTION, stream);
-        const bool cluster = pl.cluster && sp.topk == 1;
-        e = lf::launch_decode_step(s.d, g, pl.stages, a.score, cluster, tmK, tmV, sp, units, stream);
+        NvtxRange range(r.score ? "lf_decode_step" : "lf_decode_attention");
+        ProfScope prof(r.score ? LF_KERNEL_DECODE_STEP : LF_KERNEL_ATTENTION, stream);
+        const bool cluster = r.pl.cluster && r.sp.topk == 1;
+        e = lf::launch_decode_step(r.d, r.g, r.pl.stages, r.score, cluster, r.tmK, r.tmV, r.sp,
+                                   r.units, stream);
         if (e != cudaSuccess && cluster) {
             // A cluster that cannot be scheduled: the last-CTA merge, scoring
             // in the same kernel.
             (void)cudaGetLastError();
-            e = lf::launch_decode_step(s.d, g, 2, a.score, false, tmK, tmV, sp, units, stream);
+            e = lf::launch_decode_step(r.d, r.g, 2, r.score, false, r.tmK, r.tmV, r.sp, r.units,
+                                       stream);
         }
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");
-    if (sp.split) {
+    if (r.sp.split) {
         NvtxRange range("lf_score");
         ProfScope prof(LF_KERNEL_SCORE, stream);
-        e = lf::launch_score(g, sp, units, stream);
+        e = lf::launch_score(r.g, r.sp, r.units, stream);
         if (e != cudaSuccess) return cuda_fail(e, "scoring-kernel launch");
     }
     return LF_OK;
+}
+
+lf_status enqueue_step(const StepArgs& a, const Shape& s, cudaStream_t stream, Scratch* scr,
+                       const Layout& L, const Plan& pl) {
+    Launch r;
+    lf_status st = build_launch(a, s, static_cast<char*>(scr->base), scr->arrivals, scr->dev_err,
+                                L, pl, &r);
+    if (st != LF_OK) return st;
+    return launch(r, stream);
 }
 
 lf_status run_step(const StepArgs& a, const Shape& s, void* stream_v) {
@@ -569,6 +598,42 @@ lf_status static_scratch_base(int dev, void** out) {
     }
     *out = g_static_base[dev];
     return LF_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------- prepared steps --
+//
+// A prepared step fixes the buffers, shape and launch plan once: each run is
+// the staging copies it needs, one or two kernel launches and the copies
+// back, with no argument checks, plan, tensor-map lookup or pointer query.
+// The handle owns its scratch, counters and error word, so runs of different
+// handles never share state.
+
+struct lf_step_handle {
+    int dev = 0;
+    cudaStream_t stream = nullptr;
+    Launch r;
+    void* mem = nullptr;        // scratch, then staging for I/O buffers not addressable in place
+    uint32_t* words = nullptr;  // 4 words per unit (counters, argmin words), then the error word
+    uint32_t* dev_err = nullptr;
+    struct Copy {
+        void* dst;
+        const void* src;
+        size_t bytes;
+    };
+    Copy h2d[4];
+    int n_h2d = 0;
+    Copy d2h[2];
+    int n_d2h = 0;
+};
+
+namespace {
+
+void free_handle(lf_step_handle* h) {
+    if (h->mem) cudaFree(h->mem);
+    if (h->words) cudaFree(h->words);
+    delete h;
 }
 
 }  // namespace
@@ -776,6 +841,157 @@ lf_status lf_step_plan(int B, int Hq, int Hkv, int d, int S, int topk, int32_t* 
     plan[3] = pl.cluster ? 1 : 0;
     plan[4] = pl.split ? 1 : 0;
     plan[5] = pl.fit;
+    return LF_OK;
+}
+
+lf_status lf_step_prepare(const void* q, void* k_cache, void* v_cache, int32_t* mask,
+                          const void* new_k, const void* new_v, const int32_t* write_slot,
+                          void* out, int32_t* next_slot, int B, int Hq, int Hkv, int d, int S,
+                          int W, float scale, void* stream_v, lf_step_handle** handle) {
+    if (!handle) return fail(LF_ERR_INVALID_ARG, "handle is NULL");
+    *handle = nullptr;
+    const Shape s{B, Hq, Hkv, d, S, W, scale};
+    lf_status st;
+    if (!q || !new_k || !new_v || !write_slot || !out || !next_slot)
+        return fail(LF_ERR_INVALID_ARG, "an input or output buffer is NULL");
+    if ((st = check_ptr(k_cache, 16, "k_cache")) != LF_OK) return st;
+    if ((st = check_ptr(v_cache, 16, "v_cache")) != LF_OK) return st;
+    if ((st = check_ptr(mask, 4, "mask")) != LF_OK) return st;
+    if ((st = check_shape(s)) != LF_OK) return st;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+
+    const size_t units = static_cast<size_t>(B) * Hkv;
+    const size_t q_bytes = static_cast<size_t>(B) * Hq * d * 2;
+    const size_t kv_bytes = units * d * 2;
+    const size_t i_bytes = units * 4;
+    const Plan pl = plan_split(S, static_cast<int>(units), sm_count(dev), true, d, Hq / Hkv, true);
+    const Layout L = scratch_layout(s, pl, 0);
+
+    // Where each per-step buffer lives: device memory of this device is used
+    // as is; page-locked host memory this device can address is read and
+    // written in place (unless LF_HOST_ZEROCOPY=0); anything else is staged
+    // in the handle's device memory with a copy each way per run.
+    const char* zenv = std::getenv("LF_HOST_ZEROCOPY");
+    const bool zero_copy = !(zenv && std::atoi(zenv) == 0);
+    struct Io {
+        const void* p;
+        size_t bytes, align;
+        bool input;
+        const char* name;
+        void* dev;      // the pointer the kernel uses (null: staged)
+        size_t off;     // staging offset
+    };
+    Io io[6] = {{q, q_bytes, 16, true, "q", nullptr, 0},
+                {new_k, kv_bytes, 16, true, "new_k", nullptr, 0},
+                {new_v, kv_bytes, 16, true, "new_v", nullptr, 0},
+                {write_slot, i_bytes, 4, true, "write_slot", nullptr, 0},
+                {out, q_bytes, 16, false, "out", nullptr, 0},
+                {next_slot, i_bytes, 4, false, "next_slot", nullptr, 0}};
+    size_t staging = align_up(L.total, 256);
+    for (Io& b : io) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, b.p) != cudaSuccess) {
+            (void)cudaGetLastError();
+            at.type = cudaMemoryTypeUnregistered;
+        }
+        if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+            if (at.device != dev)
+                return fail(LF_ERR_INVALID_ARG, "%s is memory of device %d, not of the current device %d",
+                            b.name, at.device, dev);
+            if (!aligned(b.p, b.align))
+                return fail(LF_ERR_INVALID_ARG, "%s is not %zu-byte aligned", b.name, b.align);
+            b.dev = const_cast<void*>(b.p);
+        } else if (zero_copy && at.type == cudaMemoryTypeHost && at.devicePointer &&
+                   aligned(at.devicePointer, b.align)) {
+            b.dev = at.devicePointer;
+        } else {
+            b.off = staging;
+            staging = align_up(staging + b.bytes, 256);
+        }
+    }
+
+    lf_step_handle* h = new (std::nothrow) lf_step_handle;
+    if (!h) return fail(LF_ERR_NO_MEMORY, "out of host memory");
+    h->dev = dev;
+    h->stream = static_cast<cudaStream_t>(stream_v);
+    if ((e = cudaMalloc(&h->mem, staging)) != cudaSuccess) {
+        h->mem = nullptr;
+        free_handle(h);
+        return fail(LF_ERR_NO_MEMORY, "cudaMalloc(%zu bytes of scratch): %s", staging,
+                    cudaGetErrorString(e));
+    }
+    const size_t words = 4 * units + 64;
+    if ((e = cudaMalloc(&h->words, words * sizeof(uint32_t))) != cudaSuccess) {
+        h->words = nullptr;
+        free_handle(h);
+        return fail(LF_ERR_NO_MEMORY, "cudaMalloc(counters): %s", cudaGetErrorString(e));
+    }
+    if ((e = cudaMemset(h->words, 0, words * sizeof(uint32_t))) != cudaSuccess) {
+        free_handle(h);
+        return cuda_fail(e, "cudaMemset");
+    }
+    h->dev_err = h->words + 4 * units;
+    char* base = static_cast<char*>(h->mem);
+    for (Io& b : io) {
+        if (b.dev) continue;
+        b.dev = base + b.off;
+        if (b.input)
+            h->h2d[h->n_h2d++] = {b.dev, b.p, b.bytes};
+        else
+            h->d2h[h->n_d2h++] = {const_cast<void*>(b.p), b.dev, b.bytes};
+    }
+    const StepArgs a{io[0].dev, k_cache, v_cache, mask, io[1].dev, io[2].dev,
+                     static_cast<const int32_t*>(io[3].dev), io[4].dev,
+                     static_cast<int32_t*>(io[5].dev), nullptr};
+    if ((st = build_launch(a, s, base, h->words, h->dev_err, L, pl, &h->r)) != LF_OK) {
+        free_handle(h);
+        return st;
+    }
+    *handle = h;
+    return LF_OK;
+}
+
+lf_status lf_step_run(lf_step_handle* h) {
+    if (!h) return fail(LF_ERR_INVALID_ARG, "handle is NULL");
+    cudaError_t e;
+    for (int i = 0; i < h->n_h2d; ++i)
+        if ((e = cudaMemcpyAsync(h->h2d[i].dst, h->h2d[i].src, h->h2d[i].bytes,
+                                 cudaMemcpyHostToDevice, h->stream)) != cudaSuccess)
+            return cuda_fail(e, "host-to-device copy");
+    lf_status st = launch(h->r, h->stream);
+    if (st != LF_OK) return st;
+    for (int i = 0; i < h->n_d2h; ++i)
+        if ((e = cudaMemcpyAsync(h->d2h[i].dst, h->d2h[i].src, h->d2h[i].bytes,
+                                 cudaMemcpyDeviceToHost, h->stream)) != cudaSuccess)
+            return cuda_fail(e, "device-to-host copy");
+    return LF_OK;
+}
+
+lf_status lf_step_errors(lf_step_handle* h, uint32_t* flags, int clear) {
+    if (!h || !flags) return fail(LF_ERR_INVALID_ARG, "handle or flags is NULL");
+    *flags = 0;
+    uint32_t v = 0;
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(&v, h->dev_err, sizeof v, cudaMemcpyDeviceToHost, h->stream)) != cudaSuccess)
+        return cuda_fail(e, "reading the device error word");
+    if ((e = cudaStreamSynchronize(h->stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    *flags = v;
+    if (clear && v) {
+        if ((e = cudaMemsetAsync(h->dev_err, 0, sizeof v, h->stream)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemsetAsync");
+        if ((e = cudaStreamSynchronize(h->stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    }
+    return LF_OK;
+}
+
+lf_status lf_step_destroy(lf_step_handle* h) {
+    if (!h) return LF_OK;
+    // Work queued on the handle's stream may still use its memory.
+    cudaError_t e = cudaStreamSynchronize(h->stream);
+    free_handle(h);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     return LF_OK;
 }
 

@@ -234,6 +234,46 @@ lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, in
                                  void* stream);
 
 /*
+ * Prepared steps: lf_decode_step (top-1, score on) with its buffers, shape,
+ * launch plan and stream fixed once, for a serving loop that runs the same
+ * layer's step token after token. lf_step_prepare checks the arguments
+ * (errors as for lf_decode_step), takes the plan and the K/V tensor maps,
+ * and resolves where each per-step buffer lives: q, new_k, new_v,
+ * write_slot, out and next_slot may each be device memory of the current
+ * device (used as is), page-locked host memory the device can address (read
+ * and written by the kernel in place, as lf_decode_step_host does) or any
+ * other host memory (staged through the handle's device memory, one copy
+ * each way per run). k_cache, v_cache and mask are device memory.
+ *   - The handle owns its scratch, counters and error word (about
+ *     B * Hkv * S * (Hq / Hkv) * 4 bytes of per-slot score terms plus
+ *     partials); no other call or handle shares them.
+ *   - The handle keeps the pointers: the buffers must outlive it, and their
+ *     contents are read and written at each run (the caller writes the next
+ *     token's inputs into the same buffers; next_slot of one run is usually
+ *     the write_slot buffer of the next, through a second handle whose
+ *     write_slot and next_slot buffers are swapped).
+ *   - lf_step_run enqueues one step on the prepare-time stream with the
+ *     prepare-time device current: the staging copies, one or two kernel
+ *     launches (two with the split finish), the copies back. No argument
+ *     checks, allocation, plan or pointer queries: the cost of the call is
+ *     the launches. Runs of one handle must not overlap (they share its
+ *     scratch); they may be captured in a CUDA graph on that stream.
+ *   - LF_* switches are read at prepare time.
+ *   - lf_step_errors reads (and with clear != 0 clears) the handle's device
+ *     error word (LF_DEVERR_* bits), synchronising its stream.
+ *   - lf_step_destroy synchronises the stream and frees the handle (NULL is
+ *     a no-op).
+ */
+typedef struct lf_step_handle lf_step_handle;
+lf_status lf_step_prepare(const void* q, void* k_cache, void* v_cache, int32_t* mask,
+                          const void* new_k, const void* new_v, const int32_t* write_slot,
+                          void* out, int32_t* next_slot, int B, int Hq, int Hkv, int d, int S,
+                          int W, float scale, void* stream, lf_step_handle** handle);
+lf_status lf_step_run(lf_step_handle* handle);
+lf_status lf_step_errors(lf_step_handle* handle, uint32_t* flags, int clear);
+lf_status lf_step_destroy(lf_step_handle* handle);
+
+/*
  * Read (and optionally clear) the device error word of `stream`'s scratch.
  * Synchronises the stream. *flags receives an OR of LF_DEVERR_* bits, 0 if the
  * stream has never run a step.

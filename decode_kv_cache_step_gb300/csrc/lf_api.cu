@@ -767,8 +767,10 @@ lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, in
     const size_t units = static_cast<size_t>(B) * Hkv;
     const Plan pl = plan_split(S, static_cast<int>(units), sms > 0 ? sms : 1, true, d, Hq / Hkv, true);
     const Layout L = scratch_layout(s, pl, 0);
+    // Per unit 4 words: the chunk and scoring-kernel arrival counters and the
+    // 64-bit argmin word of a split finish.
     const size_t arrivals_off = align_up(L.total, 256);
-    const size_t err_off = align_up(arrivals_off + units * sizeof(uint32_t), 256);
+    const size_t err_off = align_up(arrivals_off + 4 * units * sizeof(uint32_t), 256);
     const size_t need = err_off + 256;
     if (need > kStaticScratchBytes)
         return fail(LF_ERR_UNSUPPORTED,
@@ -781,47 +783,12 @@ lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, in
     // The arrival counters and the error word must start at zero.
     if ((e = cudaMemsetAsync(base + arrivals_off, 0, need - arrivals_off, stream)) != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync(static scratch)");
-
-    const int g = Hq / Hkv;
-    CUtensorMap tmK, tmV;
-    if ((st = encode_cache_map(&tmK, k_cache, d, S, static_cast<int>(units))) != LF_OK) return st;
-    if ((st = encode_cache_map(&tmV, v_cache, d, S, static_cast<int>(units))) != LF_OK) return st;
-    lf::StepParams sp;
-    sp.q = static_cast<const __nv_bfloat16*>(q);
-    sp.k_cache = static_cast<__nv_bfloat16*>(k_cache);
-    sp.v_cache = static_cast<__nv_bfloat16*>(v_cache);
-    sp.mask = mask;
-    sp.new_k = static_cast<const __nv_bfloat16*>(new_k);
-    sp.new_v = static_cast<const __nv_bfloat16*>(new_v);
-    sp.write_slot = write_slot;
-    sp.out = static_cast<__nv_bfloat16*>(out);
-    sp.next_slot = next_slot;
-    sp.scores = nullptr;
-    sp.part_o = reinterpret_cast<float*>(base + L.o);
-    sp.part_ml = reinterpret_cast<float2*>(base + L.ml);
-    sp.stash = reinterpret_cast<float*>(base + L.stash);
-    sp.arrivals = reinterpret_cast<uint32_t*>(base + arrivals_off);
-    sp.dev_err = reinterpret_cast<uint32_t*>(base + err_off);
-    sp.Hq = Hq;
-    sp.Hkv = Hkv;
-    sp.S = S;
-    sp.W = W;
-    sp.nchunk = pl.nchunk;
-    sp.chunk_tiles = pl.chunk_tiles;
-    sp.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    Launch r;
+    if ((st = build_launch(a, s, base, reinterpret_cast<uint32_t*>(base + arrivals_off),
+                           reinterpret_cast<uint32_t*>(base + err_off), L, pl, &r)) != LF_OK)
+        return st;
     g_last_error[0] = '\0';
-    sp.topk = 1;
-    sp.flags = 0;
-    sp.wait_limit_ns = wait_limit_ns();
-    e = lf::launch_decode_step(d, g, pl.stages, true, pl.cluster, tmK, tmV, sp,
-                               static_cast<int>(units), stream);
-    if (e != cudaSuccess && pl.cluster) {
-        (void)cudaGetLastError();
-        e = lf::launch_decode_step(d, g, 2, true, false, tmK, tmV, sp, static_cast<int>(units),
-                                   stream);
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");
-    return LF_OK;
+    return launch(r, stream);
 }
 
 lf_status lf_step_plan(int B, int Hq, int Hkv, int d, int S, int topk, int32_t* plan) {

@@ -14,12 +14,14 @@ first failure has already run every other test.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 import decode_kv_cache_step_gb300 as lf
 from decode_kv_cache_step_gb300.workloads import WORKLOADS, initial_state, step_inputs
 
+import _pins
 from _gpu import OUT_ATOL, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -63,6 +65,33 @@ def test_noalloc_matches_lf_decode_step_on_two_calls_in_a_row():
             assert (ws_got >= 0).all()  # the second call really wrote new tokens
         ws_ref.copy_(nxt_ref)
         ws_got.copy_(nxt_got)
+
+
+@pytest.mark.parametrize("cluster", ["0", "1"])
+def test_noalloc_long_units(monkeypatch, cluster):
+    """9000-slot units: clusters of 16, or (clusters off) the last-CTA merge
+    with the split finish's scoring kernel, from the static scratch."""
+    monkeypatch.setenv("LF_CLUSTER", cluster)
+    rng = np.random.default_rng(12)
+    case = _pins.rand_case(rng, 2, 8, 2, 128, 9000, p_masked=0.2, max_age=20000)
+    W, scale = 8, 0.088
+    p = lf.step_plan(2, 8, 2, 128, 9000)
+    assert p["split"] == (cluster == "0")
+    dc = {kk: to_dev(vv) for kk, vv in case.items()}
+    ref_mask = dc["mask"].clone()
+    ref_k, ref_v = dc["k_cache"].clone(), dc["v_cache"].clone()
+    out_ref = torch.empty((2, 8, 128), dtype=torch.bfloat16, device="cuda")
+    out_got = torch.empty_like(out_ref)
+    nxt_ref = torch.empty((2, 2), dtype=torch.int32, device="cuda")
+    nxt_got = torch.empty_like(nxt_ref)
+    lf.decode_step(dc["q"], ref_k, ref_v, ref_mask, dc["new_k"], dc["new_v"], dc["write_slot"],
+                   out_ref, nxt_ref, W, scale)
+    lf.decode_step_noalloc(dc["q"], dc["k_cache"], dc["v_cache"], dc["mask"], dc["new_k"],
+                           dc["new_v"], dc["write_slot"], out_got, nxt_got, W, scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out_got, out_ref) and torch.equal(nxt_got, nxt_ref)
+    assert torch.equal(dc["mask"], ref_mask)
+    assert torch.equal(dc["k_cache"], ref_k) and torch.equal(dc["v_cache"], ref_v)
 
 
 def test_noalloc_refuses_a_shape_whose_scratch_does_not_fit():

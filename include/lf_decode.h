@@ -44,7 +44,7 @@
  *   - The library owns a per-(device, stream) scratch buffer that it grows on
  *     demand with cudaMalloc (released by lf_release_workspace). Calls on the
  *     same stream are ordered; calls on different streams use different
- *     scratch.
+ *     scratch. A prepared step (lf_step_prepare) owns its own scratch.
  *   - Argument errors are detected on the host before anything is enqueued;
  *     the kernels never trap.
  *

@@ -258,7 +258,9 @@ lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, in
  *     checks, allocation, plan or pointer queries: the cost of the call is
  *     the launches. Runs of one handle must not overlap (they share its
  *     scratch); they may be captured in a CUDA graph on that stream.
- *   - LF_* switches are read at prepare time.
+ *   - LF_* switches are read at prepare time. lf_step_prepare allocates
+ *     (cudaMalloc, cudaMemset) and lf_step_destroy synchronises: call both
+ *     outside any stream capture.
  *   - lf_step_errors reads (and with clear != 0 clears) the handle's device
  *     error word (LF_DEVERR_* bits), synchronising its stream.
  *   - lf_step_destroy synchronises the stream and frees the handle (NULL is

@@ -1,7 +1,8 @@
 // Instantiations of the decode-step kernel whose unit runs as one
-// thread-block cluster (one-wave grids): a 2-stage TMA ring at three CTAs
-// per SM, or a kDeepStages ring at one CTA per SM that keeps every tile of a
-// short chunk in flight at once when the grid has at most one CTA per SM.
+// thread-block cluster (grids whose clusters are all resident at once): a
+// 2-stage TMA ring at three CTAs per SM, or a kDeepStages ring at one CTA per
+// SM that keeps every tile of a short chunk in flight at once. Also the
+// cluster-residency query the launch plan relies on.
 #include <atomic>
 
 #include "lf_step_kernel.cuh"

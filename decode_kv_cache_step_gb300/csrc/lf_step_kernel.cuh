@@ -43,9 +43,11 @@
 // the scan to a second kernel (the split finish, lf_score_kernel in
 // lf_decode_step.cu) that scores every chunk of every unit in parallel once
 // the step's memory traffic is over. Shorter ragged units scan only the tiles
-// that hold a live slot (top-1; the chunk CTAs publish their live-tile masks). When the whole grid fits in one wave, a unit's chunks run as
-// one thread-block cluster instead (kCluster): they merge through distributed
-// shared memory and each CTA scores its own chunk (top-1 only). A cluster
+// that hold a live slot (top-1; the chunk CTAs publish their live-tile
+// masks). When every unit's cluster (up to 16 CTAs) can be resident at once,
+// a unit's chunks run as one thread-block cluster instead (kCluster): they
+// merge through distributed shared memory and each CTA scores its own chunk
+// (top-1 only). A cluster
 // grid of at most one CTA per SM uses a kDeepStages-deep TMA ring, so every
 // tile of a short chunk is in flight at once.
 // An attention-only instantiation (kScore = false) drops the row norms, the
@@ -1019,7 +1021,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     allow_dependent_launch();
     grid_dependency_wait();
 
-    // In the one-wave cluster variant (latency-bound) the write slot, q and
+    // In the cluster variant (small, latency-bound grids) the write slot, q and
     // the chunk's mask are all loaded before the slot is checked, so they
     // share one round trip; large grids check it first (measured faster).
     int ws = p.write_slot[u];

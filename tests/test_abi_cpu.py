@@ -96,3 +96,39 @@ def test_profile_api_without_launches(lib):
     lf.profile_enable(False)
     with pytest.raises(lf.LFError):
         lf.profile_collect(7)
+
+
+def test_prepared_step_and_plan_validate_on_the_host(lib):
+    h = ctypes.c_void_p(0)
+    args = [FAKE] * 9 + [1, 4, 2, 128, 16, 2, ctypes.c_float(0.1), None]
+    assert lib.lf_step_prepare(*args, None) == lf.LF_ERR_INVALID_ARG          # no handle slot
+    bad = list(args)
+    bad[0] = None                                                             # q missing
+    assert lib.lf_step_prepare(*bad, ctypes.byref(h)) == lf.LF_ERR_INVALID_ARG
+    bad = list(args)
+    bad[1] = FAKE + 8                                                         # misaligned k_cache
+    assert lib.lf_step_prepare(*bad, ctypes.byref(h)) == lf.LF_ERR_INVALID_ARG
+    bad = list(args)
+    bad[12] = 96                                                              # head dim 96
+    assert lib.lf_step_prepare(*bad, ctypes.byref(h)) == lf.LF_ERR_UNSUPPORTED
+    assert h.value is None
+    assert lib.lf_step_run(None) == lf.LF_ERR_INVALID_ARG
+    assert lib.lf_step_errors(None, None, 0) == lf.LF_ERR_INVALID_ARG
+    assert lib.lf_step_destroy(None) == lf.LF_OK
+    plan = (ctypes.c_int32 * 6)()
+    assert lib.lf_step_plan(1, 4, 2, 128, 16, 1, None) == lf.LF_ERR_INVALID_ARG
+    assert lib.lf_step_plan(1, 6, 4, 128, 16, 1, plan) == lf.LF_ERR_INVALID_ARG
+    assert lib.lf_step_plan(1, 4, 2, 128, 16, 0, plan) == lf.LF_ERR_INVALID_ARG
+    assert lib.lf_step_plan(1, 4, 2, 96, 16, 1, plan) == lf.LF_ERR_UNSUPPORTED
+
+
+def test_prepared_step_binding_checks_tensors():
+    import torch
+    bf = torch.bfloat16
+    q = torch.zeros(1, 4, 64, dtype=bf)
+    k = torch.zeros(1, 2, 16, 64, dtype=bf)            # host caches: refused before the ABI
+    mask = torch.zeros(1, 2, 16, dtype=torch.int32)
+    nk = torch.zeros(1, 2, 64, dtype=bf)
+    ws = torch.zeros(1, 2, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        lf.PreparedStep(q, k, k, mask, nk, nk, ws, q, ws, 2, 0.1)

@@ -327,9 +327,9 @@ Plan plan_split(int S, int units, int sms, bool want_cluster, int D, int G, bool
             // cluster (longer chunks, at most kMaxChunkTiles tiles) whose
             // clusters are all resident at once. Measured against the
             // last-CTA plan: the 3200-slot Qwen3 shape at batch 8, 6 chunks of
-            // 9 tiles in clusters 22.1 us per step against 29.9 for 10 of 5;
-            // at batch 16, 3 of 17 in clusters 40.5 against 50.1 for 4 of 13;
-            // four 16K-slot sequences, 10 of 26 in clusters 44.1 against 58.7
+            // 9 tiles in clusters 22.4 us per step against 29.9 for 10 of 5;
+            // at batch 16, 3 of 17 in clusters 38.2 against 50.1 for 4 of 13;
+            // four 16K-slot sequences, 12 of 22 in clusters 45.6 against 58.7
             // for 20 of 13 with the split finish.
             for (int n2 = nc - 1; n2 >= 1; --n2) {
                 const int ct2 = (pl.tiles + n2 - 1) / n2;

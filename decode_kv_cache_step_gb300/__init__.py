@@ -13,7 +13,8 @@ from ._binding import (  # noqa: F401
     EXPORTED, KERNEL_NAMES, LF_DEVERR_BAD_WRITE_SLOT, LF_DEVERR_WAIT_TIMEOUT,
     LF_ERR_CUDA, LF_ERR_INVALID_ARG, LF_ERR_NO_MEMORY, LF_ERR_UNSUPPORTED,
     LF_KERNEL_ATTENTION, LF_KERNEL_DECODE_STEP, LF_KERNEL_SCORE, LF_MAX_TOPK, LF_OK,
-    LF_STEP_FILL_EMPTY_FIRST, LF_STEP_MASK_EVICTED, LFError, PreparedStep, decode_attention,
+    LF_STEP_FILL_EMPTY_FIRST, LF_STEP_LOG2_SCORES, LF_STEP_MASK_EVICTED, LFError, PreparedStep,
+    decode_attention,
     decode_step, decode_step_ex,
     decode_step_host, decode_step_noalloc,
     decode_step_scores, device_errors, library_path, load_library, profile_collect,

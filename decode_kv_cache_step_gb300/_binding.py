@@ -34,6 +34,7 @@ KERNEL_NAMES = {LF_KERNEL_DECODE_STEP: "lf_decode_step_kernel",
 
 LF_STEP_FILL_EMPTY_FIRST = 0x1
 LF_STEP_MASK_EVICTED = 0x2
+LF_STEP_LOG2_SCORES = 0x4
 LF_MAX_TOPK = 1024
 
 # Every exported symbol of include/lf_decode.h.
@@ -206,7 +207,8 @@ def decode_step_scores(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out,
 def decode_step_ex(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out, next_slots, W,
                    scale, k=1, flags=0, scores=None, stream=None):
     """lf_decode_step_ex: next_slots [B,Hkv,k] int32 gets the k lowest-(score, slot)
-    candidates per unit; flags are LF_STEP_* bits; scores optional [B,Hkv,S]."""
+    candidates per unit; flags are LF_STEP_* bits; scores optional [B,Hkv,S]
+    (log2 I_j with LF_STEP_LOG2_SCORES)."""
     lib = load_library()
     B, Hq, Hkv, d, S = _check_step(q, k_cache, v_cache, mask, new_k, new_v, write_slot, out,
                                    next_slots, k=k)

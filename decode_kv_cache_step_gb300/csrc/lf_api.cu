@@ -22,6 +22,12 @@
 namespace {
 
 constexpr int kVersion = 100;  // 0.1.0
+
+// The header's step flags are the kernel's flag bits.
+static_assert(LF_STEP_FILL_EMPTY_FIRST == lf::kFlagFillEmptyFirst &&
+                  LF_STEP_MASK_EVICTED == lf::kFlagMaskEvicted &&
+                  LF_STEP_LOG2_SCORES == lf::kFlagLog2Scores,
+              "step flag bits");
 constexpr int kMaxNChunk = 1024;
 constexpr int kMaxS = 1 << 20;
 
@@ -431,7 +437,7 @@ lf_status check_args(const StepArgs& a, const Shape& s) {
     if (a.scores && !aligned(a.scores, 4)) return fail(LF_ERR_INVALID_ARG, "scores is not 4-byte aligned");
     if (a.topk < 1 || a.topk > LF_MAX_TOPK)
         return fail(LF_ERR_INVALID_ARG, "k = %d is outside [1, %d]", a.topk, LF_MAX_TOPK);
-    if (a.flags & ~(LF_STEP_FILL_EMPTY_FIRST | LF_STEP_MASK_EVICTED))
+    if (a.flags & ~(LF_STEP_FILL_EMPTY_FIRST | LF_STEP_MASK_EVICTED | LF_STEP_LOG2_SCORES))
         return fail(LF_ERR_INVALID_ARG, "unknown flag bits 0x%x", a.flags);
     return check_shape(s);
 }

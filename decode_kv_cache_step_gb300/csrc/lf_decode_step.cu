@@ -14,11 +14,12 @@ namespace {
 // memory system. With a split finish the decode-step kernel stops after the
 // merge (publishing c_h per unit) and this kernel, launched behind it with
 // programmatic dependent launch, scores every chunk of every unit in
-// parallel: I_j = sum_h 2^(t_hj + c_h), the same arithmetic in the same order
-// as the single-kernel scan, so scores and choices are bit-identical. The
-// lexicographic (I_j, j) argmin is an atomic maximum over the complemented
-// 64-bit key (score bits + 1, slot), empty slots (fill-empty-first) taking
-// score key 0; the last CTA of the unit reads and clears it.
+// parallel: log2 I_j from the terms t_hj + c_h, the same arithmetic in the
+// same order as the single-kernel scan, so scores and choices are
+// bit-identical. The lexicographic (I_j, j) argmin is an atomic maximum over
+// the complemented 64-bit key (ordered log2 I_j, slot), empty slots
+// (fill-empty-first) taking score key 0; the last CTA of the unit reads and
+// clears it.
 constexpr int kScoreThreads = 128;
 constexpr int kScoreWarps = kScoreThreads / 32;
 constexpr int kScoreTilesPerWarp = 2;  // tiles a warp loads per round trip (4 slots per lane)
@@ -62,8 +63,9 @@ __global__ void __launch_bounds__(kScoreThreads, G >= 8 ? 4 : 8) lf_score_kernel
 
     // Each lane keeps its best (score key, slot). A lane visits its slots in
     // increasing order, so a strict "<" on the key alone keeps the lowest slot
-    // among equal keys. Key: score bits + 1 (I >= 0, so the bits order like
-    // the values), 0 for an empty slot under fill-empty-first, ~0u for none.
+    // among equal keys. Key: ordered_key(log2 I_j) (the order of the scores
+    // at any scale, below fp32's normal range included), 0 for an empty slot
+    // under fill-empty-first, ~0u for none.
     uint32_t bkey = 0xffffffffu;
     int bj = 0x7fffffff;
     const int tlo = c0 * ct;
@@ -98,17 +100,16 @@ __global__ void __launch_bounds__(kScoreThreads, G >= 8 ? 4 : 8) lf_score_kernel
             for (int r = 0; r < 2; ++r) {
                 const int j = (tb + q) * kTile + r * 32 + lane;
                 const int aa = a[2 * q + r];
-                float I = 0.f;
-#pragma unroll
-                for (int h = 0; h < G; ++h) I += ex2_approx(t[2 * q + r][h] + cf[h]);
+                const float L = log2_score<G>(t[2 * q + r], cf);
                 const bool live = aa >= 0;
-                const bool cand = live ? (aa >= W && I == I) : fill_first;
-                const uint32_t key = live ? __float_as_uint(I) + 1u : 0u;
+                const bool cand = live ? (aa >= W && L == L) : fill_first;
+                const uint32_t key = live ? ordered_key(L) : 0u;
                 if (cand && j < S && key < bkey) {
                     bkey = key;
                     bj = j;
                 }
-                if (scores && j < S) scores[j] = live ? I : INFINITY;
+                if (scores && j < S)
+                    scores[j] = live ? exported_score<G>(p, L, t[2 * q + r], cf) : INFINITY;
             }
         }
     }

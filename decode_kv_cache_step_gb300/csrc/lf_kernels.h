@@ -53,6 +53,7 @@ struct StepParams {
 
 constexpr int kFlagFillEmptyFirst = 1;  // empty (masked) slots are returned before any score
 constexpr int kFlagMaskEvicted = 2;     // returned slots are masked (-1) in place
+constexpr int kFlagLog2Scores = 4;      // the score export holds log2 I_j
 constexpr int kMaxTopK = 1024;
 constexpr int kMaxClusterChunks = 16;   // chunks of a unit run as one cluster up to this
                                         // (above 8: a non-portable cluster size)

@@ -34,9 +34,12 @@
 // LongFlowScore for every live slot, selects the slots to evict and drops the
 // unit's scratch lines from L2 without writing them back. The selection is
 // the lexicographic (I_j, j) argmin over slots with age >= W, or, for k > 1,
-// the k smallest by an 8-bit radix select on the score bits (then on the slot
+// the k smallest by an 8-bit radix select on the score keys (then on the slot
 // index among equal scores) and a bitonic sort of the k winners; the periodic
-// k-at-once compression of the Fig. 3 caption. Empty slots can rank first
+// k-at-once compression of the Fig. 3 caption. Candidates are compared by an
+// order-preserving key of log2 I_j, so slots whose scores lie far below
+// fp32's normal range (weights hundreds of nats under the unit's maximum)
+// are still told apart. Empty slots can rank first
 // (cache-fill phase) and the chosen slots can be masked in place.
 // Long units stream their score terms through shared memory with bulk copies
 // for that scan, or, for top-1 steps over units of thousands of slots, leave
@@ -117,8 +120,55 @@ __device__ __forceinline__ uint32_t swz_off(int row, int cg) {
     return (cg >> 3) * kBoxBytes + row * 128 + (((cg & 7) ^ (row & 7)) << 4);
 }
 
-__device__ __forceinline__ bool better(float v, int j, float bv, int bj) {
-    return v < bv || (v == bv && j < bj);
+// log2 I_j of a live slot from its score terms, x_h = t_hj + c_h:
+// I_j = sum_h 2^(x_h) = 2^M * sum_h 2^(x_h - M) with M = max_h x_h, so
+// log2 I_j = M + log2(sum_h 2^(x_h - M)), the sum in [1, g]. fp32 holds this
+// far below the range where I_j itself flushes to zero (a slot whose weight
+// is hundreds of nats under the unit's maximum still has its own value).
+// -inf for a zero score (every term -inf: a zero V row); NaN propagates. The
+// "+ 0" turns a -0 into +0, so equal values have equal keys.
+template <int G>
+__device__ __forceinline__ float log2_score(const float (&t)[G], const float (&c)[G]) {
+    float x[G];
+    float M = -INFINITY;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        x[h] = t[h] + c[h];
+        M = fmaxf(M, x[h]);
+    }
+    const float Mu = (M == -INFINITY || M == INFINITY) ? 0.f : M;
+    float s = 0.f;
+#pragma unroll
+    for (int h = 0; h < G; ++h) s += ex2_approx(x[h] - Mu);
+    return Mu + __log2f(s) + 0.f;
+}
+
+// The linear score I_j = sum_h 2^(x_h) in fp32 (0 once below the normal
+// range), for the score export.
+template <int G>
+__device__ __forceinline__ float linear_score(const float (&t)[G], const float (&c)[G]) {
+    float I = 0.f;
+#pragma unroll
+    for (int h = 0; h < G; ++h) I += ex2_approx(t[h] + c[h]);
+    return I;
+}
+
+// Selection key of a live slot: the bits of log2 I_j mapped so that unsigned
+// order is float order (negative values complemented, the sign bit set on
+// the others). -inf maps to 0x007fffff and +inf to 0xff800000, which leaves
+// key 0 for an empty slot ranked first (fill-empty-first) and 0xffffffff for
+// "no candidate".
+__device__ __forceinline__ uint32_t ordered_key(float v) {
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// What the score export holds for a live slot: I_j, or log2 I_j with
+// kFlagLog2Scores.
+template <int G>
+__device__ __forceinline__ float exported_score(const StepParams& p, float L, const float (&t)[G],
+                                                const float (&c)[G]) {
+    return (p.flags & kFlagLog2Scores) ? L : linear_score<G>(t, c);
 }
 
 template <int G>
@@ -517,19 +567,17 @@ __device__ void score_and_select(const StepParams& p, int u, const float* s_m, c
     // only when empty slots are candidates or every score is wanted.
     const bool all = fill_first || scores != nullptr;
     const int W = p.W;
-    // Selection key of a candidate: the score's bits + 1 (I >= 0 orders like
-    // its bits), 0 for an empty slot under fill-empty-first; ~0u: none.
+    // Selection key of a candidate: ordered_key(log2 I_j), 0 for an empty
+    // slot under fill-empty-first; ~0u: none.
     uint32_t bkey = 0xffffffffu;  // top-1: this thread's best (key, slot)
     int bestj = 0x7fffffff;
     int ncand = 0;
 
-    auto visit = [&](int j, int a, const float* t) {
-        float I = 0.f;
-#pragma unroll
-        for (int h = 0; h < G; ++h) I += ex2_approx(t[h] + c[h]);
+    auto visit = [&](int j, int a, const float (&t)[G]) {
+        const float L = log2_score<G>(t, c);
         const bool live = a >= 0;
-        const bool cand = live ? (a >= W && I == I) : fill_first;
-        const uint32_t key = live ? __float_as_uint(I) + 1u : 0u;
+        const bool cand = live ? (a >= W && L == L) : fill_first;
+        const uint32_t key = live ? ordered_key(L) : 0u;
         if (top1) {
             // A thread visits its slots in increasing order, so a strict "<"
             // keeps the lowest slot among equal keys.
@@ -541,7 +589,7 @@ __device__ void score_and_select(const StepParams& p, int u, const float* s_m, c
             keys[static_cast<size_t>(j) * G] = cand ? key : 0xffffffffu;
             ncand += cand ? 1 : 0;
         }
-        if (scores) scores[j] = live ? I : INFINITY;
+        if (scores) scores[j] = live ? exported_score<G>(p, L, t, c) : INFINITY;
     };
 
     if (!all && !top1) {
@@ -772,8 +820,8 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
                   "cluster epilogue arrays exceed the TMA ring");
     float* pub_o = reinterpret_cast<float*>(smem + ((kWBytes + 15) & ~15));  // [G][D]
     float2* pub_ml = reinterpret_cast<float2*>(pub_o + G * D);               // [G]
-    // Every CTA's local best, written into rank 0's copy of these arrays.
-    float* pub_best = reinterpret_cast<float*>(pub_ml + G);                  // [16]
+    // Every CTA's local best (key, slot), written into rank 0's copy of these arrays.
+    uint32_t* pub_best = reinterpret_cast<uint32_t*>(pub_ml + G);            // [16]
     int* pub_bestj = reinterpret_cast<int*>(pub_best + kMaxClusterChunks);   // [16]
     float2* s_mlc = reinterpret_cast<float2*>(pub_bestj + kMaxClusterChunks);  // [nchunk][G]
     float* s_w = reinterpret_cast<float*>(s_mlc + kMaxClusterChunks * G);    // [nchunk][G]
@@ -887,8 +935,8 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
         const bool fill_first = (p.flags & kFlagFillEmptyFirst) != 0;
         const int W = p.W;
         // A thread visits its slots in increasing order, so a strict "<" on
-        // the key (score bits + 1; 0 for an empty slot under fill-empty-first)
-        // keeps the lowest slot among equal keys.
+        // the key (ordered_key(log2 I_j); 0 for an empty slot under
+        // fill-empty-first) keeps the lowest slot among equal keys.
         uint32_t bkey = 0xffffffffu;
         int bestj = 0x7fffffff;
         for (int i0 = tid; i0 < n; i0 += kBatch * kConsumers) {
@@ -912,43 +960,39 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
                 if (i >= n) break;
                 const int a = ages[i];
                 const int j = slot0 + i;
-                float I = 0.f;
-#pragma unroll
-                for (int h = 0; h < G; ++h) I += ex2_approx(t[k][h] + cexp[h]);
+                const float L = log2_score<G>(t[k], cexp);
                 const bool live = a >= 0;
-                const bool cand = live ? (a >= W && I == I) : fill_first;
-                const uint32_t key = live ? __float_as_uint(I) + 1u : 0u;
+                const bool cand = live ? (a >= W && L == L) : fill_first;
+                const uint32_t key = live ? ordered_key(L) : 0u;
                 if (cand && key < bkey) {
                     bkey = key;
                     bestj = j;
                 }
-                if (scores) scores[j] = live ? I : INFINITY;
+                if (scores) scores[j] = live ? exported_score<G>(p, L, t[k], cexp) : INFINITY;
             }
         }
-        // Back to the (value, slot) form the cluster's reduction compares.
-        float best = bkey == 0xffffffffu ? INFINITY
-                                         : (bkey == 0u ? -1.f : __uint_as_float(bkey - 1u));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, best, off);
+            const uint32_t ok = __shfl_xor_sync(0xffffffffu, bkey, off);
             const int oj = __shfl_xor_sync(0xffffffffu, bestj, off);
-            if (better(ov, oj, best, bestj)) {
-                best = ov;
+            if (key_less(ok, oj, bkey, bestj)) {
+                bkey = ok;
                 bestj = oj;
             }
         }
+        uint32_t* red_k = reinterpret_cast<uint32_t*>(red_v);
         if ((tid & 31) == 0) {
-            red_v[tid >> 5] = best;
+            red_k[tid >> 5] = bkey;
             red_j[tid >> 5] = bestj;
         }
         consumer_bar_sync();
         if (tid == 0) {
             for (int w = 1; w < kConsumerWarps; ++w)
-                if (better(red_v[w], red_j[w], best, bestj)) {
-                    best = red_v[w];
+                if (key_less(red_k[w], red_j[w], bkey, bestj)) {
+                    bkey = red_k[w];
                     bestj = red_j[w];
                 }
-            st_dsmem_f32(dsmem_addr(&pub_best[rank], 0u), best);
+            st_dsmem_s32(dsmem_addr(&pub_best[rank], 0u), static_cast<int32_t>(bkey));
             st_dsmem_s32(dsmem_addr(&pub_bestj[rank], 0u), bestj);
         }
         // This chunk's score terms are read: drop them from L2, no write-back.
@@ -961,11 +1005,11 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
     cluster_sync();
 
     if (kScore && rank == 0 && tid == 0) {
-        float best = INFINITY;
+        uint32_t bkey = 0xffffffffu;
         int bestj = 0x7fffffff;
         for (int c = 0; c < nchunk; ++c) {
-            if (better(pub_best[c], pub_bestj[c], best, bestj)) {
-                best = pub_best[c];
+            if (key_less(pub_best[c], pub_bestj[c], bkey, bestj)) {
+                bkey = pub_best[c];
                 bestj = pub_bestj[c];
             }
         }

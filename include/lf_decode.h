@@ -107,6 +107,7 @@ typedef enum lf_status {
 /* Flags of lf_decode_step_ex. */
 #define LF_STEP_FILL_EMPTY_FIRST 0x1 /* return empty (masked) slots, lowest first, before any score */
 #define LF_STEP_MASK_EVICTED 0x2     /* mask (-1) the returned slots in place */
+#define LF_STEP_LOG2_SCORES 0x4      /* the score export holds log2 I_j instead of I_j */
 #define LF_MAX_TOPK 1024             /* largest k of lf_decode_step_ex */
 
 /*
@@ -134,6 +135,11 @@ lf_status lf_decode_step(const void* q, void* k_cache, void* v_cache, int32_t* m
  * lf_decode_step plus the per-slot LongFlowScore, for inspection and tests.
  * scores out float [B][Hkv][S]: I_j on every live slot (protected ones
  * included), +inf on masked slots. Same semantics otherwise.
+ * I_j is fp32: a score below its normal range (about 1.2e-38, a slot whose
+ * weight lies some 87 nats or more under the unit's maximum logit) reads 0.
+ * The selection does not depend on that: every entry point ranks candidates
+ * by log2 I_j, which fp32 holds at any such scale, and lf_decode_step_ex
+ * with LF_STEP_LOG2_SCORES exports those values.
  */
 lf_status lf_decode_step_scores(const void* q, void* k_cache, void* v_cache, int32_t* mask,
                                 const void* new_k, const void* new_v,
@@ -156,6 +162,8 @@ lf_status lf_decode_step_scores(const void* q, void* k_cache, void* v_cache, int
  *        before evicting (the cache-fill phase before the budget is full).
  *        LF_STEP_MASK_EVICTED: set the mask of every returned slot to -1, so
  *        it is not attended again until a later step writes into it.
+ *        LF_STEP_LOG2_SCORES: scores holds log2 I_j on live slots (-inf for
+ *        a zero score) instead of I_j; masked slots still read +inf.
  * scores optional float [B][Hkv][S] as in lf_decode_step_scores (NULL = none).
  * The other arguments are those of lf_decode_step. A combination of k and
  * slot-axis split that does not fit in shared memory returns

@@ -183,7 +183,7 @@ def test_selection_argument_errors():
     nk = torch.zeros(1, 2, 64, dtype=torch.bfloat16, device=dev)
     ws = torch.zeros(1, 2, dtype=torch.int32, device=dev)
     out = torch.zeros_like(q)
-    for kk, flags in ((0, 0), (lf.LF_MAX_TOPK + 1, 0), (1, 4)):
+    for kk, flags in ((0, 0), (lf.LF_MAX_TOPK + 1, 0), (1, 8)):  # 8: no such flag bit
         nxt = torch.zeros(1, 2, max(kk, 1), dtype=torch.int32, device=dev)
         lib = lf.load_library()
         rc = lib.lf_decode_step_ex(q.data_ptr(), k.data_ptr(), k.clone().data_ptr(),

@@ -38,7 +38,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 from decode_kv_cache_step_gb300.workloads import (  # noqa: E402
-    WORKLOADS, algorithmic_bytes, initial_state, live_lengths, sequence_state, step_inputs)
+    WORKLOADS, algorithmic_bytes, initial_state, live_lengths, step_inputs)
 
 METRIC = "decode steps/s and achieved HBM GB/s (% of GB300 peak) for fused attn+score+evict"
 DEFAULT_WORKLOAD = "qwen3_8b_b128_s3200"
@@ -207,54 +207,63 @@ def run_oracle_steps(wl, state, max_seconds: float, max_steps: int, units=None, 
 
 
 def bench_reference(args, wl):
-    """The fp64 CPU oracle on the host cores, on a bounded sample of units per step."""
+    """The fp64 CPU oracle on the host cores. Each timed step is a whole step
+    (every (b, kvh) unit) when the K steps fit in --reference-seconds at the
+    warm-up steps' rate; otherwise each step runs the same sample of units,
+    sized to fit, and the line says so."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     import oracle
     oracle.build()
-    sample_units = min(wl.units, max(1, args.reference_units))
-    rng = np.random.default_rng(0)
-    units = np.sort(rng.choice(wl.units, size=sample_units, replace=False)).astype(np.int32)
-    seqs = sorted({int(u) // wl.Hkv for u in units})
-    # Host state with only the sampled sequences filled (the oracle touches only them).
-    k = np.zeros((wl.B, wl.Hkv, wl.S, wl.d), dtype=np.uint16)
-    v = np.zeros_like(k)
-    mask = np.full((wl.B, wl.Hkv, wl.S), -1, dtype=np.int32)
-    for b in seqs:
-        k[b], v[b], mask[b], _ = sequence_state(wl, b)
-    state = {"k_cache": k, "v_cache": v, "mask": mask}
+    st = initial_state(wl)
+    k, v, mask = st["k_cache"], st["v_cache"], st["mask"]
     ws = np.full((wl.B, wl.Hkv), -1, dtype=np.int32)
 
-    def one(step):
+    def one(step, units=None):
         nonlocal ws
         inp = step_inputs(wl, step)
         res = oracle.decode_step(inp["q"], k, v, mask, inp["new_k"], inp["new_v"], ws, wl.W,
                                  wl.scale, units=units)
         nxt = res["next_slot"].copy()
-        nxt[nxt < -1] = -1
+        nxt[nxt < -1] = -1  # units outside a sample: no write at the next step
         ws = nxt
 
-    for s in range(args.warmup):
+    warm = []
+    for s in range(max(1, args.warmup)):
+        t0 = time.perf_counter()
         one(s)
+        warm.append(time.perf_counter() - t0)
+    full_s = statistics.median(warm)
+    units = None
+    if args.steps * full_s > args.reference_seconds:
+        n = max(1, int(wl.units * args.reference_seconds / (args.steps * full_s)))
+        rng = np.random.default_rng(0)
+        units = np.sort(rng.choice(wl.units, size=min(n, wl.units), replace=False)).astype(np.int32)
     t0 = time.perf_counter()
     for s in range(args.steps):
-        one(args.warmup + s)
+        one(max(1, args.warmup) + s, units)
     dt = time.perf_counter() - t0
-    scale_to_full = wl.units / sample_units
-    sec_per_step = dt / args.steps * scale_to_full
+    if units is None:
+        sec_per_step = dt / args.steps
+        sample = (f"{args.steps} whole decode steps (all {wl.units} (b,kvh) units each), "
+                  f"after {max(1, args.warmup)} whole warm-up steps")
+    else:
+        sec_per_step = dt / args.steps * wl.units / units.size
+        sample = (f"{units.size} of {wl.units} (b,kvh) units per step (the whole steps would "
+                  f"not fit in {args.reference_seconds:.0f} s), time scaled by "
+                  f"{wl.units / units.size:.1f} to a full step")
     value = 1.0 / sec_per_step
     cores = oracle.max_threads()
-    sample = (f"{sample_units} of {wl.units} (b,kvh) units per step, scaled by "
-              f"{scale_to_full:.1f} to a full step")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(wl, world),
+        "timed_region_s": dt,
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -617,8 +626,9 @@ def main():
     ap.add_argument("--batch", type=int, default=None,
                     help="run the first BATCH sequences of the workload (small profiling cases)")
     ap.add_argument("--impl", default="lf", choices=["lf", "reference"])
-    ap.add_argument("--reference-units", type=int, default=64,
-                    help="(b,kvh) units the reference arm runs per step")
+    ap.add_argument("--reference-seconds", type=float, default=150.0,
+                    help="--impl reference: time budget of the K timed oracle steps; whole "
+                         "steps when they fit, else a sample of units per step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="OpenMP threads of the CPU baseline (0: all)")

@@ -588,6 +588,10 @@ lf_status run_step(const StepArgs& a, const Shape& s, void* stream_v) {
 // cudaGetSymbolAddress, once per device, with that device current.
 constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+// The array's last 256 bytes hold the entry point's device error word. It
+// starts at zero with the module, every call ORs into it and none clears it;
+// lf_device_errors reads (and may clear) it.
+constexpr size_t kStaticErrOff = kStaticScratchBytes - 256;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
@@ -776,22 +780,22 @@ lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, in
     // Per unit 4 words: the chunk and scoring-kernel arrival counters and the
     // 64-bit argmin word of a split finish.
     const size_t arrivals_off = align_up(L.total, 256);
-    const size_t err_off = align_up(arrivals_off + 4 * units * sizeof(uint32_t), 256);
-    const size_t need = err_off + 256;
-    if (need > kStaticScratchBytes)
+    const size_t need = arrivals_off + 4 * units * sizeof(uint32_t);
+    if (need + (kStaticScratchBytes - kStaticErrOff) > kStaticScratchBytes)
         return fail(LF_ERR_UNSUPPORTED,
                     "lf_decode_step_noalloc: this shape needs %zu bytes of scratch but the static "
                     "scratch holds %zu; use lf_decode_step or fewer B * Hkv * S slots",
-                    need, kStaticScratchBytes);
+                    need + (kStaticScratchBytes - kStaticErrOff), kStaticScratchBytes);
     void* base_v = nullptr;
     if ((st = static_scratch_base(dev, &base_v)) != LF_OK) return st;
     char* base = static_cast<char*>(base_v);
-    // The arrival counters and the error word must start at zero.
+    // The arrival counters must start at zero (the kernels leave them so, but
+    // a call that timed out may not have).
     if ((e = cudaMemsetAsync(base + arrivals_off, 0, need - arrivals_off, stream)) != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync(static scratch)");
     Launch r;
     if ((st = build_launch(a, s, base, reinterpret_cast<uint32_t*>(base + arrivals_off),
-                           reinterpret_cast<uint32_t*>(base + err_off), L, pl, &r)) != LF_OK)
+                           reinterpret_cast<uint32_t*>(base + kStaticErrOff), L, pl, &r)) != LF_OK)
         return st;
     g_last_error[0] = '\0';
     return launch(r, stream);
@@ -975,21 +979,31 @@ lf_status lf_device_errors(void* stream_v, uint32_t* flags, int clear) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    uint32_t* word = nullptr;
+    // The word of the stream's scratch, and that of the allocation-free
+    // entry point's static array once it has run on this device.
+    uint32_t* words[2] = {nullptr, nullptr};
     {
         std::lock_guard<std::mutex> lock(g_mu);
         auto it = g_scratch.find({dev, stream});
-        if (it == g_scratch.end() || !it->second.dev_err) return LF_OK;
-        word = it->second.dev_err;
+        if (it != g_scratch.end()) words[0] = it->second.dev_err;
     }
-    uint32_t v = 0;
-    if ((e = cudaMemcpyAsync(&v, word, sizeof v, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
-        return cuda_fail(e, "reading the device error word");
-    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    *flags = v;
-    if (clear && v) {
-        if ((e = cudaMemsetAsync(word, 0, sizeof v, stream)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    if (dev >= 0 && dev < kMaxDevices) {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        if (g_static_base[dev])
+            words[1] = reinterpret_cast<uint32_t*>(static_cast<char*>(g_static_base[dev]) +
+                                                   kStaticErrOff);
+    }
+    for (uint32_t* word : words) {
+        if (!word) continue;
+        uint32_t v = 0;
+        if ((e = cudaMemcpyAsync(&v, word, sizeof v, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+            return cuda_fail(e, "reading the device error word");
         if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+        *flags |= v;
+        if (clear && v) {
+            if ((e = cudaMemsetAsync(word, 0, sizeof v, stream)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+            if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+        }
     }
     return LF_OK;
 }

@@ -232,8 +232,10 @@ lf_status lf_decode_step_host(const void* q_host, void* k_cache, void* v_cache, 
  *   - All calls on a device share the one array; calls whose work overlaps on
  *     the GPU (other streams, other host threads) race and corrupt each other.
  *     Serialise them on one stream. Each call zeroes the counters it needs.
- *   - Device error bits (an ignored out-of-range write_slot) stay in the
- *     static array and are not reported by lf_device_errors.
+ *   - Device error bits (an ignored out-of-range write_slot, a pipeline wait
+ *     that gave up) go to one error word in the static array, shared by every
+ *     call on the device and never cleared by a call: lf_device_errors,
+ *     given the stream these calls ran on, reports (and may clear) them.
  */
 lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, int32_t* mask,
                                  const void* new_k, const void* new_v,
@@ -284,9 +286,11 @@ lf_status lf_step_errors(lf_step_handle* handle, uint32_t* flags, int clear);
 lf_status lf_step_destroy(lf_step_handle* handle);
 
 /*
- * Read (and optionally clear) the device error word of `stream`'s scratch.
- * Synchronises the stream. *flags receives an OR of LF_DEVERR_* bits, 0 if the
- * stream has never run a step.
+ * Read (and optionally clear) the device error word of `stream`'s scratch
+ * and, on the current device, the error word of lf_decode_step_noalloc's
+ * static array (once that entry point has run there). Both are read through
+ * `stream` after synchronising it, so pass the stream the steps ran on.
+ * *flags receives an OR of LF_DEVERR_* bits, 0 if no step has set one.
  */
 lf_status lf_device_errors(void* stream, uint32_t* flags, int clear);
 

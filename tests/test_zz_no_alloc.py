@@ -7,7 +7,10 @@ that cudaMalloc and cudaFree can cause. lf_decode_step_noalloc serves them by
 keeping its scratch in a fixed array compiled into the library. These tests
 call it through the C ABI and check that two calls in a row give the same
 result as the allocating entry point, within the tolerances the other GPU
-tests use, and that a shape whose scratch does not fit is refused.
+tests use, that several steps in a row match the fp64 oracle directly, that
+its device error bits (an ignored write slot, a pipeline wait that gave up)
+reach the caller through lf_device_errors, and that a shape whose scratch
+does not fit is refused.
 
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.
@@ -22,7 +25,7 @@ import decode_kv_cache_step_gb300 as lf
 from decode_kv_cache_step_gb300.workloads import WORKLOADS, initial_state, step_inputs
 
 import _pins
-from _gpu import OUT_ATOL, to_dev
+from _gpu import OUT_ATOL, compare_unit, oracle_step, to_dev, to_host_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -115,3 +118,94 @@ def test_noalloc_refuses_a_shape_whose_scratch_does_not_fit():
         ctypes.c_float(0.088), torch.cuda.current_stream().cuda_stream)
     assert rc == lf.LF_ERR_UNSUPPORTED
     assert "static scratch" in lib.lf_last_error().decode()
+
+
+def test_noalloc_matches_the_oracle_step_after_step():
+    """Six steps of four 3200-slot Qwen3 sequences through the static scratch,
+    each compared with the oracle on every unit: output, next_slot, and the
+    cache and mask bits. Both sides write the oracle's chosen slot."""
+    wl = WORKLOADS["qwen3_8b_b128_s3200"].with_batch(4)
+    st = initial_state(wl)
+    host = {kk: st[kk] for kk in ("k_cache", "v_cache", "mask")}
+    dev = _state(st)
+    out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.bfloat16, device="cuda")
+    nxt = torch.empty((wl.B, wl.Hkv), dtype=torch.int32, device="cuda")
+    ws = np.full((wl.B, wl.Hkv), -1, dtype=np.int32)
+    lf.device_errors(clear=True)
+    for t in range(6):
+        inp = step_inputs(wl, t)
+        lf.decode_step_noalloc(to_dev(inp["q"]), dev["k"], dev["v"], dev["mask"],
+                               to_dev(inp["new_k"]), to_dev(inp["new_v"]), to_dev(ws), out, nxt,
+                               wl.W, wl.scale)
+        torch.cuda.synchronize()
+        ora = oracle_step(host, inp["q"], inp["new_k"], inp["new_v"], ws, wl.W, wl.scale)
+        gpu = {"out": out.float().cpu().numpy().astype(np.float64),
+               "next_slot": nxt.cpu().numpy()}
+        assert np.array_equal(dev["mask"].cpu().numpy(), host["mask"]), f"step {t}: mask"
+        assert np.array_equal(to_host_bits(dev["k"]), host["k_cache"]), f"step {t}: k_cache"
+        assert np.array_equal(to_host_bits(dev["v"]), host["v_cache"]), f"step {t}: v_cache"
+        for u in range(wl.units):
+            b, kvh = divmod(u, wl.Hkv)
+            compare_unit(gpu, ora, b, kvh, wl.g, host["mask"], wl.W, check_scores=False,
+                         where=f"noalloc step {t}")
+        ws = ora["next_slot"].astype(np.int32).copy()
+    assert lf.device_errors(clear=True) == 0
+
+
+def test_noalloc_reports_an_ignored_write_slot():
+    """An out-of-range write slot is ignored (the rest of the step is
+    correct) and its bit reaches lf_device_errors; clearing it leaves the word
+    at zero for the next call."""
+    rng = np.random.default_rng(41)
+    case = _pins.rand_case(rng, 2, 8, 2, 128, 500, p_masked=0.1, max_age=2000)
+    case["write_slot"][1, 0] = 500 + 7
+    lf.device_errors(clear=True)
+    dc = {kk: to_dev(vv) for kk, vv in case.items()}
+    out = torch.empty((2, 8, 128), dtype=torch.bfloat16, device="cuda")
+    nxt = torch.empty((2, 2), dtype=torch.int32, device="cuda")
+    lf.decode_step_noalloc(dc["q"], dc["k_cache"], dc["v_cache"], dc["mask"], dc["new_k"],
+                           dc["new_v"], dc["write_slot"], out, nxt, 8, 0.088)
+    flags = lf.device_errors(clear=True)
+    assert flags == lf.LF_DEVERR_BAD_WRITE_SLOT
+    host = {kk: np.array(case[kk], copy=True) for kk in ("k_cache", "v_cache", "mask")}
+    ws = case["write_slot"].copy()
+    ws[1, 0] = -1  # what the kernel does with it: no write, nothing ages
+    ora = oracle_step(host, case["q"], case["new_k"], case["new_v"], ws, 8, 0.088)
+    assert np.array_equal(dc["mask"].cpu().numpy(), host["mask"])
+    gpu = {"out": out.float().cpu().numpy().astype(np.float64), "next_slot": nxt.cpu().numpy()}
+    for b in range(2):
+        for h in range(2):
+            compare_unit(gpu, ora, b, h, 4, host["mask"], 8, check_scores=False, where="bad slot")
+    assert lf.device_errors(clear=True) == 0
+
+
+def test_noalloc_reports_a_wait_timeout(monkeypatch):
+    """With the pipeline waits cut to 1 ns (LF_WAIT_LIMIT_NS, a diagnostic),
+    the waits give up before the copies land: the bit must reach
+    lf_device_errors, and the next call with the normal limit must be right."""
+    rng = np.random.default_rng(43)
+    case = _pins.rand_case(rng, 4, 32, 8, 128, 2000, p_masked=0.1, max_age=5000)
+    lf.device_errors(clear=True)
+    monkeypatch.setenv("LF_WAIT_LIMIT_NS", "1")
+    dc = {kk: to_dev(vv) for kk, vv in case.items()}
+    out = torch.empty((4, 32, 128), dtype=torch.bfloat16, device="cuda")
+    nxt = torch.empty((4, 8), dtype=torch.int32, device="cuda")
+    lf.decode_step_noalloc(dc["q"], dc["k_cache"], dc["v_cache"], dc["mask"], dc["new_k"],
+                           dc["new_v"], dc["write_slot"], out, nxt, 16, 0.088)
+    flags = lf.device_errors(clear=True)
+    assert flags & lf.LF_DEVERR_WAIT_TIMEOUT
+    monkeypatch.delenv("LF_WAIT_LIMIT_NS")
+    dc = {kk: to_dev(vv) for kk, vv in case.items()}
+    lf.decode_step_noalloc(dc["q"], dc["k_cache"], dc["v_cache"], dc["mask"], dc["new_k"],
+                           dc["new_v"], dc["write_slot"], out, nxt, 16, 0.088)
+    torch.cuda.synchronize()
+    host = {kk: np.array(case[kk], copy=True) for kk in ("k_cache", "v_cache", "mask")}
+    ora = oracle_step(host, case["q"], case["new_k"], case["new_v"], case["write_slot"], 16,
+                      0.088)
+    assert np.array_equal(dc["mask"].cpu().numpy(), host["mask"])
+    gpu = {"out": out.float().cpu().numpy().astype(np.float64), "next_slot": nxt.cpu().numpy()}
+    for b in range(4):
+        for h in range(8):
+            compare_unit(gpu, ora, b, h, 4, host["mask"], 16, check_scores=False,
+                         where="after a timed-out call")
+    assert lf.device_errors(clear=True) == 0

@@ -49,6 +49,10 @@ struct StepParams {
     int flags;                   // kFlag* bits
     // Limit of the pipeline waits; drains of copies in flight always allow 1 s.
     uint64_t wait_limit_ns;
+    // CTAs whose linear index is below this issue their chunk's first tiles
+    // before the mask tells which tiles hold a live slot (the grid's first
+    // wave; set by the launch).
+    int spec_ctas = 0;
 };
 
 constexpr int kFlagFillEmptyFirst = 1;  // empty (masked) slots are returned before any score
@@ -92,5 +96,6 @@ int max_active_clusters(int D, int G, int stages, bool score, int csize);
 // scores chunk c of unit u from the ages, the score terms and c_h, and the
 // unit's last CTA writes next_slot (and masks it with kFlagMaskEvicted).
 cudaError_t launch_score(int G, const StepParams& p, int units, cudaStream_t stream);
+
 
 }  // namespace lf

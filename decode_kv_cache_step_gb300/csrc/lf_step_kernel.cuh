@@ -60,6 +60,7 @@
 // one before its first global read.
 #pragma once
 
+#include <limits.h>
 #include <math.h>
 #include <stdlib.h>
 
@@ -1033,7 +1034,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     int32_t* ages = reinterpret_cast<int32_t*>(smem + L::kAgesOff);
     int32_t* list = reinterpret_cast<int32_t*>(smem + L::kListOff);
-    // [0] live tile count, [1] abort flag, [2] last-CTA flag
+    // [0] tiles in ring order, [1] abort flag, [2] last-CTA flag, [3] live tile count
     volatile int32_t* misc = reinterpret_cast<int32_t*>(smem + L::kMiscOff);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
     uint64_t* empty = full + kStages;
@@ -1057,6 +1058,9 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         misc[1] = 0;
         fence_barrier_init();
     }
+    // The barriers are initialised before any thread may use them (the
+    // producer can issue copies before the prologue's barriers below).
+    __syncthreads();
     // With programmatic dependent launch this CTA may start while the previous
     // kernel of the stream (often the previous decode step) is still running:
     // everything above touches only this CTA's shared memory; every global
@@ -1065,14 +1069,33 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     allow_dependent_launch();
     grid_dependency_wait();
 
-    // In the cluster variant (small, latency-bound grids) the write slot, q and
-    // the chunk's mask are all loaded before the slot is checked, so they
-    // share one round trip; large grids check it first (measured faster).
-    int ws = p.write_slot[u];
-    if (!kCluster && (ws < -1 || ws >= S)) {
-        if (tid == 0 && chunk == 0) atomicOr(p.dev_err, LF_DEVERR_BAD_WRITE_SLOT);
-        ws = -1;
+    // Speculative first tiles. The CTAs of the grid's first wave all start
+    // here at once, when nothing else streams: they issue their chunk's first
+    // nspec tiles before the mask round trip tells which tiles hold a live
+    // slot, so the copies overlap it (a dead tile among them is processed as
+    // fully masked and contributes nothing, so the results are the same bits).
+    // Later CTAs start while their SM's other CTAs stream, and wait for the
+    // live-tile list instead. Cluster grids are a single wave: all speculate.
+    const int lin = static_cast<int>(blockIdx.y) * static_cast<int>(gridDim.x) + chunk;
+    const int nspec = (lin < p.spec_ctas) ? min(kStages, ntiles) : 0;
+    if (warp == kConsumerWarps && lane == 0) {
+        const uint64_t pol = l2_policy_evict_first();
+        for (int i = 0; i < nspec; ++i) {
+            uint8_t* kb = smem + i * L::kStageBytes;
+            uint8_t* vb = kb + L::kTensorBytes;
+            mbar_arrive_expect_tx(&full[i], L::kStageBytes);
+            const int y = slot0 + i * kTile;
+#pragma unroll
+            for (int bx = 0; bx < L::kBoxes; ++bx) {
+                tma_load_3d(kb + bx * L::kBoxBytes, &tmK, bx * kBoxCols, y, u, &full[i], pol);
+                tma_load_3d(vb + bx * L::kBoxBytes, &tmV, bx * kBoxCols, y, u, &full[i], pol);
+            }
+        }
     }
+
+    // The write slot, q and the chunk's mask are all loaded before the slot
+    // is checked, so they share one round trip.
+    int ws = p.write_slot[u];
 
     // Q^T as the B operand of S^T = K . Q^T, loaded early so its latency
     // overlaps the mask prologue: b0 = (d = 16kk + h0 .. +1, head r), b1 = d + 8.
@@ -1112,7 +1135,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         const int i = tid + k * kConsumers;
         av[k] = (ager && i < n) ? mrow[i] : -1;
     }
-    if (kCluster && (ws < -1 || ws >= S)) {
+    if (ws < -1 || ws >= S) {
         if (tid == 0 && chunk == 0) atomicOr(p.dev_err, LF_DEVERR_BAD_WRITE_SLOT);
         ws = -1;
     }
@@ -1136,37 +1159,44 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     __syncthreads();
 
     // Tiles with no live slot are never loaded (ragged fills stream only
-    // their live part).
-    // The same list, as a bit mask, tells the unit's last CTA which tiles
-    // its score scan can skip.
+    // their live part), apart from speculative ones. The ring order: the
+    // nspec speculative tiles, then the other live tiles in increasing order.
+    // The live tiles, as a bit mask, tell the unit's last CTA which tiles its
+    // score scan can skip.
     if (warp == 0) {
+        int nlist = 0;
         int cnt = 0;
         uint32_t bits = 0u;
         for (int t = 0; t < ntiles; ++t) {
             const int i0 = t * kTile + lane;
             const int i1 = i0 + 32;
-            const bool live = (i0 < n && ages[i0] >= 0) || (i1 < n && ages[i1] >= 0);
-            if (__any_sync(0xffffffffu, live)) {
-                if (lane == 0) list[cnt] = t;
+            const bool live = __any_sync(0xffffffffu, (i0 < n && ages[i0] >= 0) || (i1 < n && ages[i1] >= 0));
+            if (live) {
                 bits |= 1u << t;
                 ++cnt;
             }
+            if (live || t < nspec) {
+                if (lane == 0) list[nlist] = t;
+                ++nlist;
+            }
         }
         if (lane == 0) {
-            misc[0] = cnt;
+            misc[0] = nlist;
+            misc[3] = cnt;
             if (kScore && !kCluster && p.part_tiles && !p.split)
                 p.part_tiles[static_cast<size_t>(u) * p.nchunk + chunk] = bits;
         }
     }
     __syncthreads();
-    const int cnt = misc[0];
+    const int nlist = misc[0];  // tiles the ring delivers
+    const int cnt = misc[3];    // tiles holding a live slot
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------ producer --
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            int issued = 0;
-            for (int i = 0; i < cnt; ++i) {
+            int issued = nspec;
+            for (int i = nspec; i < nlist; ++i) {
                 const int s = i % kStages;
                 if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, p.wait_limit_ns)) {
                     atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
@@ -1209,7 +1239,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     const float sl = p.scale_log2;
     const int wrow0 = warp * 16;
 
-    for (int i = 0; i < cnt; ++i) {
+    for (int i = 0; i < nlist; ++i) {
         const int s = i % kStages;
         if (!mbar_wait(&full[s], (i / kStages) & 1, p.wait_limit_ns)) {
             if (lane == 0) atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
@@ -1478,15 +1508,47 @@ int max_active_clusters_t(int csize) {
     return n;
 }
 
+// How many CTAs of the (non-cluster) instance are resident at once on the
+// current device: the grid's first wave. Cached per device.
+template <int D, int G, int kStages, bool kScore>
+int first_wave_t() {
+    static int cached_for = -1;
+    static int ctas = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cached_for != dev) {
+        int per_sm = 0, sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &per_sm, lf_decode_step_kernel<D, G, kStages, kScore, false>, kThreads,
+                StepSmem<D, kStages>::kAlloc) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        ctas = per_sm * sms;
+        cached_for = dev;
+    }
+    return ctas;
+}
+
 template <int D, int G, int kStages, bool kScore, bool kCluster>
-cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p,
+cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepParams& p_in,
                      int units, cudaStream_t stream, bool pdl) {
     using L = StepSmem<D, kStages>;
-    if (finish_smem_bytes(p.nchunk, G, kScore ? p.topk : 1) > static_cast<size_t>(L::kBarOff))
+    if (finish_smem_bytes(p_in.nchunk, G, kScore ? p_in.topk : 1) > static_cast<size_t>(L::kBarOff))
         return cudaErrorInvalidConfiguration;
     auto kernel = lf_decode_step_kernel<D, G, kStages, kScore, kCluster>;
     cudaError_t e = configure_t<D, G, kStages, kScore, kCluster>();
     if (e != cudaSuccess) return e;
+    // Speculative first tiles in the first wave (LF_SPEC=0: off; cluster
+    // grids, one wave by construction, always speculate).
+    StepParams p = p_in;
+    const char* spec_env = std::getenv("LF_SPEC");
+    const bool spec = !(spec_env && std::atoi(spec_env) == 0);
+    if constexpr (kCluster)
+        p.spec_ctas = spec ? INT_MAX : 0;
+    else
+        p.spec_ctas = spec ? first_wave_t<D, G, kStages, kScore>() : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.nchunk, units);
     cfg.blockDim = dim3(kThreads);

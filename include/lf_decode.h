@@ -53,7 +53,7 @@
  *
  * Environment switches, read at every call (tuning and tests; every setting
  * stays within the same tolerances of the exact result, and LF_SPLIT,
- * LF_SCORE_PARTS and LF_PDL change no result bit):
+ * LF_SCORE_PARTS, LF_SPEC and LF_PDL change no result bit):
  *   LF_CHUNK_TILES=n   64-slot tiles per chunk of the slot axis (1..32);
  *                      a cluster merge may still re-chunk to its size cap
  *   LF_STAGES=3        three-stage TMA ring (two CTAs per SM) instead of two
@@ -64,6 +64,8 @@
  *                      2-stage TMA ring / take the deep one even for chunks
  *                      of fewer than 5 tiles
  *   LF_PDL=0           programmatic dependent launch off
+ *   LF_SPEC=0          the grid's first wave waits for the live-tile list
+ *                      before loading tiles (no speculative first tiles)
  *   LF_SPLIT=0|1       split finish off / on for every top-1 step without
  *                      clusters (default: units of at least 8192 slots)
  *   LF_SCORE_PARTS=n   scoring-kernel CTAs per unit in a split finish

@@ -83,3 +83,49 @@ def test_live_tile_scan_matches_oracle(monkeypatch, chunk_tiles, entry):
             if entry == "ex_evict" and got[b, h] >= 0:
                 want[got[b, h]] = -1
             assert np.array_equal(mask_gpu[b, h], want), f"unit ({b},{h}) mask"
+
+
+def _run_bits(case, W, scale, scores=False):
+    dc = {k: to_dev(v) for k, v in case.items()}
+    B, Hq, d = case["q"].shape
+    Hkv, S = case["k_cache"].shape[1], case["k_cache"].shape[2]
+    out = torch.empty((B, Hq, d), dtype=torch.bfloat16, device="cuda")
+    nxt = torch.full((B, Hkv), -7, dtype=torch.int32, device="cuda")
+    sc = torch.empty((B, Hkv, S), dtype=torch.float32, device="cuda") if scores else None
+    args = (dc["q"], dc["k_cache"], dc["v_cache"], dc["mask"], dc["new_k"], dc["new_v"],
+            dc["write_slot"], out, nxt)
+    if scores:
+        lf.decode_step_scores(*args, sc, W, scale)
+    else:
+        lf.decode_step(*args, W, scale)
+    torch.cuda.synchronize()
+    assert lf.device_errors() == 0
+    res = [out.view(torch.int16).cpu(), nxt.cpu(), dc["mask"].cpu(),
+           dc["k_cache"].view(torch.int16).cpu(), dc["v_cache"].view(torch.int16).cpu()]
+    if scores:
+        res.append(sc.cpu())
+    return res
+
+
+@pytest.mark.parametrize("plan", ["last_cta", "cluster", "split", "deep"])
+@pytest.mark.parametrize("scores", [False, True])
+def test_speculative_first_tiles_change_no_bit(monkeypatch, plan, scores):
+    """The first wave's CTAs issue their chunk's first tiles before the mask
+    says which are live; a dead one is processed as fully masked. Ragged
+    units with dead chunks, holes and writes into dead tiles give the same
+    bits with speculation off (LF_SPEC=0), on every merge path."""
+    env = {"last_cta": {"LF_CLUSTER": "0", "LF_SPLIT": "0"},
+           "cluster": {"LF_CLUSTER": "1", "LF_DEEP": "0"},
+           "split": {"LF_CLUSTER": "0", "LF_SPLIT": "1"},
+           "deep": {"LF_CLUSTER": "1", "LF_DEEP": "1"}}[plan]
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    S, W, scale = 1000, 8, 0.088
+    case = _case(23, S, PATTERNS, WRITES)
+    on = _run_bits(case, W, scale, scores)
+    monkeypatch.setenv("LF_SPEC", "0")
+    off = _run_bits(case, W, scale, scores)
+    for a, b in zip(on, off):
+        assert torch.equal(a, b)
+    ora = _pins.run(oracle.decode_step, case, W, scale, want_scores=True)
+    assert np.max(np.abs(on[0].view(torch.bfloat16).float().numpy() - ora["out"])) <= OUT_ATOL

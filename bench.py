@@ -557,7 +557,8 @@ def bench_lf(args, wl):
     alg_launch = algorithmic_bytes(wl, lengths)
     alg = alg_launch * L
     # A split finish adds the scoring kernel to every step: the roofline then
-    # covers both kernels of the step (their summed event times).
+    # covers both kernels of the step (one event pair around the two, which
+    # overlap; the scoring kernel has no time of its own).
     split = launches_per_layer > 1
     kern_avg_ms = (kern_ms + score_ms) / max(kern_n, 1)
     peaks, peak_kind = measured_peaks()

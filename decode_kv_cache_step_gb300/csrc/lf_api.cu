@@ -57,7 +57,8 @@ struct Scratch {
     uint32_t* dev_err = nullptr;   // never moves once created
     // Per unit, zero between steps: the decode-step kernel's chunk arrival
     // counters [units], the scoring kernel's [units], its 64-bit argmin
-    // words [units] (4 words per unit in all).
+    // words [units], the ready flags [units] (lf::kCounterWordsPerUnit
+    // words per unit in all).
     uint32_t* arrivals = nullptr;
     size_t arrivals_len = 0;
 };
@@ -76,9 +77,10 @@ lf_status get_scratch(int dev, cudaStream_t stream, size_t need, size_t units, S
             s.arrivals = nullptr;
             s.arrivals_len = 0;
         }
-        cudaError_t e = cudaMalloc(&s.arrivals, 4 * units * sizeof(uint32_t));
+        const size_t words = lf::kCounterWordsPerUnit * units;
+        cudaError_t e = cudaMalloc(&s.arrivals, words * sizeof(uint32_t));
         if (e != cudaSuccess) return fail(LF_ERR_NO_MEMORY, "cudaMalloc(arrival counters): %s", cudaGetErrorString(e));
-        e = cudaMemset(s.arrivals, 0, 4 * units * sizeof(uint32_t));
+        e = cudaMemset(s.arrivals, 0, words * sizeof(uint32_t));
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
         s.arrivals_len = units;
     }
@@ -150,6 +152,13 @@ struct ProfScope {
         g_prof.push_back({kernel, start, stop});
     }
 };
+
+// Counts a launch under `kernel` without events of its own (its time is
+// inside an enclosing ProfScope).
+void prof_count(int kernel) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    if (g_prof_on) g_prof.push_back({kernel, nullptr, nullptr});
+}
 
 // ------------------------------------------------------------- device info --
 
@@ -499,6 +508,7 @@ lf_status build_launch(const StepArgs& a, const Shape& s, char* base, uint32_t* 
     sp.part_tiles = reinterpret_cast<uint32_t*>(base + L.tiles);
     sp.score_arrivals = arrivals + units;
     sp.best = reinterpret_cast<unsigned long long*>(arrivals + 2 * static_cast<size_t>(units));
+    sp.ready = arrivals + 4 * static_cast<size_t>(units);
     sp.Hq = s.Hq;
     sp.Hkv = s.Hkv;
     sp.S = s.S;
@@ -529,24 +539,25 @@ lf_status launch(const Launch& r, cudaStream_t stream) {
         ~NvtxRange() { nvtxRangePop(); }
     };
     cudaError_t e;
-    {
-        NvtxRange range(r.score ? "lf_decode_step" : "lf_decode_attention");
-        ProfScope prof(r.score ? LF_KERNEL_DECODE_STEP : LF_KERNEL_ATTENTION, stream);
-        const bool cluster = r.pl.cluster && r.sp.topk == 1;
-        e = lf::launch_decode_step(r.d, r.g, r.pl.stages, r.score, cluster, r.tmK, r.tmV, r.sp,
-                                   r.units, stream);
-        if (e != cudaSuccess && cluster) {
-            // A cluster that cannot be scheduled: the last-CTA merge, scoring
-            // in the same kernel.
-            (void)cudaGetLastError();
-            e = lf::launch_decode_step(r.d, r.g, 2, r.score, false, r.tmK, r.tmV, r.sp, r.units,
-                                       stream);
-        }
+    // A split finish's two launches are one event pair (LF_KERNEL_DECODE_STEP):
+    // an event recorded between them would end the programmatic dependency
+    // that lets the scoring kernel start during the decode-step kernel's
+    // tail. The scoring launch is counted under LF_KERNEL_SCORE.
+    NvtxRange range(r.score ? "lf_decode_step" : "lf_decode_attention");
+    ProfScope prof(r.score ? LF_KERNEL_DECODE_STEP : LF_KERNEL_ATTENTION, stream);
+    const bool cluster = r.pl.cluster && r.sp.topk == 1;
+    e = lf::launch_decode_step(r.d, r.g, r.pl.stages, r.score, cluster, r.tmK, r.tmV, r.sp,
+                               r.units, stream);
+    if (e != cudaSuccess && cluster) {
+        // A cluster that cannot be scheduled: the last-CTA merge, scoring
+        // in the same kernel.
+        (void)cudaGetLastError();
+        e = lf::launch_decode_step(r.d, r.g, 2, r.score, false, r.tmK, r.tmV, r.sp, r.units,
+                                   stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode-step launch");
     if (r.sp.split) {
-        NvtxRange range("lf_score");
-        ProfScope prof(LF_KERNEL_SCORE, stream);
+        prof_count(LF_KERNEL_SCORE);
         e = lf::launch_score(r.g, r.sp, r.units, stream);
         if (e != cudaSuccess) return cuda_fail(e, "scoring-kernel launch");
     }
@@ -625,7 +636,7 @@ struct lf_step_handle {
     cudaStream_t stream = nullptr;
     Launch r;
     void* mem = nullptr;        // scratch, then staging for I/O buffers not addressable in place
-    uint32_t* words = nullptr;  // 4 words per unit (counters, argmin words), then the error word
+    uint32_t* words = nullptr;  // counter words (lf::kCounterWordsPerUnit per unit), then the error word
     uint32_t* dev_err = nullptr;
     struct Copy {
         void* dst;
@@ -777,10 +788,10 @@ lf_status lf_decode_step_noalloc(const void* q, void* k_cache, void* v_cache, in
     const size_t units = static_cast<size_t>(B) * Hkv;
     const Plan pl = plan_split(S, static_cast<int>(units), sms > 0 ? sms : 1, true, d, Hq / Hkv, true);
     const Layout L = scratch_layout(s, pl, 0);
-    // Per unit 4 words: the chunk and scoring-kernel arrival counters and the
-    // 64-bit argmin word of a split finish.
+    // Per unit, the chunk and scoring-kernel arrival counters, the 64-bit
+    // argmin word and the ready flag of a split finish.
     const size_t arrivals_off = align_up(L.total, 256);
-    const size_t need = arrivals_off + 4 * units * sizeof(uint32_t);
+    const size_t need = arrivals_off + lf::kCounterWordsPerUnit * units * sizeof(uint32_t);
     if (need + (kStaticScratchBytes - kStaticErrOff) > kStaticScratchBytes)
         return fail(LF_ERR_UNSUPPORTED,
                     "lf_decode_step_noalloc: this shape needs %zu bytes of scratch but the static "
@@ -899,7 +910,7 @@ lf_status lf_step_prepare(const void* q, void* k_cache, void* v_cache, int32_t* 
         return fail(LF_ERR_NO_MEMORY, "cudaMalloc(%zu bytes of scratch): %s", staging,
                     cudaGetErrorString(e));
     }
-    const size_t words = 4 * units + 64;
+    const size_t words = lf::kCounterWordsPerUnit * units + 64;
     if ((e = cudaMalloc(&h->words, words * sizeof(uint32_t))) != cudaSuccess) {
         h->words = nullptr;
         free_handle(h);
@@ -909,7 +920,7 @@ lf_status lf_step_prepare(const void* q, void* k_cache, void* v_cache, int32_t* 
         free_handle(h);
         return cuda_fail(e, "cudaMemset");
     }
-    h->dev_err = h->words + 4 * units;
+    h->dev_err = h->words + lf::kCounterWordsPerUnit * units;
     char* base = static_cast<char*>(h->mem);
     for (Io& b : io) {
         if (b.dev) continue;
@@ -1026,12 +1037,13 @@ lf_status lf_profile_collect(int kernel_id, double* total_ms, int64_t* launches)
             keep.push_back(r);
             continue;
         }
+        ++n;
+        if (!r.start) continue;  // counted only
         cudaError_t e = cudaEventSynchronize(r.stop);
         float ms = 0.f;
         if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
         if (e != cudaSuccess) return cuda_fail(e, "profile event");
         sum += ms;
-        ++n;
         g_event_pool.push_back(r.start);
         g_event_pool.push_back(r.stop);
     }

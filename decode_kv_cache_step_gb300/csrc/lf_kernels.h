@@ -38,10 +38,12 @@ struct StepParams {
     uint32_t* arrivals;          // [units] chunk arrival counters, 0 between steps
     uint32_t* dev_err;           // LF_DEVERR_* bits
     // Split finish (top-1 only): the last CTA publishes c_h = log2(1/l_h) - m_h
-    // and a second kernel scores the unit's chunks in parallel.
+    // and raises the unit's ready flag; a second kernel scores the unit's
+    // chunks in parallel as soon as the flag is up.
     float* cfold = nullptr;                // [units][G]
     unsigned long long* best = nullptr;    // [units] ~(score key, slot) maximum, 0 between steps
     uint32_t* score_arrivals = nullptr;    // [units] arrival counters of the scoring kernel
+    uint32_t* ready = nullptr;             // [units] 1 once the unit is merged, 0 between steps
     int split = 0;
     int Hq, Hkv, S, W, nchunk, chunk_tiles;
     float scale_log2;            // scale * log2(e)
@@ -62,6 +64,10 @@ constexpr int kMaxTopK = 1024;
 constexpr int kMaxClusterChunks = 16;   // chunks of a unit run as one cluster up to this
                                         // (above 8: a non-portable cluster size)
 constexpr int kDeepStages = 6;          // TMA ring of the one-CTA-per-SM cluster variant
+// Counter words per unit in a step's scratch, all zero between steps: the
+// chunk arrival counter, the scoring kernel's arrival counter, the 64-bit
+// argmin word and the ready flag, each in an array of its own.
+constexpr int kCounterWordsPerUnit = 5;
 
 // Dynamic shared memory the kernel needs for head dim D and a TMA ring of
 // `stages` tiles (2 or 3).
@@ -92,9 +98,10 @@ cudaError_t launch_decode_step_cluster(int D, int G, int stages, bool score,
 // 0 if none can or the query fails. Cached per device and instance.
 int max_active_clusters(int D, int G, int stages, bool score, int csize);
 
-// The scoring kernel of a split finish: grid (nchunk, units); CTA (c, u)
-// scores chunk c of unit u from the ages, the score terms and c_h, and the
-// unit's last CTA writes next_slot (and masks it with kFlagMaskEvicted).
+// The scoring kernel of a split finish: grid (parts, units); CTA (c, u)
+// waits for unit u's ready flag, scores its chunks from the ages, the score
+// terms and c_h, and the unit's last CTA writes next_slot (and masks it with
+// kFlagMaskEvicted). It does not wait for the decode-step grid as a whole.
 cudaError_t launch_score(int G, const StepParams& p, int units, cudaStream_t stream);
 
 

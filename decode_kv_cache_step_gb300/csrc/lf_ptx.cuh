@@ -22,6 +22,18 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// 32-bit global load with acquire semantics at GPU scope.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* a) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+
+// 32-bit global store with release semantics at GPU scope.
+__device__ __forceinline__ void st_release_gpu(uint32_t* a, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -489,8 +489,16 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int usabl
     }
     if constexpr (kScore) {
         if (p.split) {
-            // The scoring kernel that follows scores the chunks in parallel.
+            // The scoring kernel that follows scores the chunks in parallel
+            // once the unit's flag is up: publish c_h, then release the flag
+            // after every write it reads (c_h, and through the arrival
+            // counter, the chunks' score terms and ages).
             if (tid < G) p.cfold[static_cast<size_t>(u) * G + tid] = __log2f(s_il[tid]) - s_m[tid];
+            consumer_bar_sync();
+            if (tid == 0) {
+                __threadfence();
+                st_release_gpu(p.ready + u, 1u);
+            }
         } else {
             score_and_select<G>(p, u, s_m, s_il, red_v, red_j, s_ncand, s_live, topk_area,
                                 scan_area, scan_bytes, scan_bars, tid);
@@ -1064,10 +1072,15 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     // With programmatic dependent launch this CTA may start while the previous
     // kernel of the stream (often the previous decode step) is still running:
     // everything above touches only this CTA's shared memory; every global
-    // read comes after the wait. The next step may begin launching as soon as
-    // every CTA of this one has started.
-    allow_dependent_launch();
+    // read comes after the wait. The next kernel may begin launching as soon
+    // as every CTA of this one has started. With a split finish, the next
+    // kernel is the scoring kernel, which watches this step's ready flags
+    // without waiting for this grid: it may start only once every CTA here
+    // has passed its own wait, so the previous step's scoring kernel (which
+    // lowers the flags) is over.
+    if (!p.split) allow_dependent_launch();
     grid_dependency_wait();
+    if (p.split) allow_dependent_launch();
 
     // Speculative first tiles. The CTAs of the grid's first wave all start
     // here at once, when nothing else streams: they issue their chunk's first

@@ -98,8 +98,9 @@ typedef enum lf_status {
  * Kernel ids for lf_profile_collect. A decode step is one launch of the
  * decode-step kernel, followed, for top-1 steps over long units (a "split
  * finish"), by one launch of the scoring kernel: the decode-step kernel then
- * stops after the merge and the scoring kernel computes LongFlowScore and the
- * argmin of every chunk in parallel.
+ * stops after each unit's merge and the scoring kernel computes LongFlowScore
+ * and the argmin of every chunk in parallel, each unit as soon as the
+ * decode-step kernel has merged it (the two kernels overlap).
  */
 #define LF_KERNEL_DECODE_STEP 0 /* slot write, mask ageing, attention (+ score, eviction) */
 #define LF_KERNEL_ATTENTION 1   /* lf_decode_attention: slot write and attention only */
@@ -315,10 +316,14 @@ lf_status lf_step_plan(int B, int Hq, int Hkv, int d, int S, int topk, int32_t* 
 
 /*
  * Kernel timing. While enabled, every kernel launch of the library is
- * bracketed by CUDA events recorded on its own stream. lf_profile_collect
- * synchronises those events and returns, for one kernel id, the summed event
- * time in milliseconds and the number of launches since the last collect for
- * that id, then forgets them.
+ * bracketed by CUDA events recorded on its own stream, except that a split
+ * finish's two launches share one pair: its time, from the decode-step
+ * kernel's start to the scoring kernel's end, is reported under
+ * LF_KERNEL_DECODE_STEP, and the scoring launch is counted under
+ * LF_KERNEL_SCORE with no time of its own (events between the two would
+ * serialise them). lf_profile_collect synchronises the events and returns,
+ * for one kernel id, the summed event time in milliseconds and the number of
+ * launches since the last collect for that id, then forgets them.
  */
 lf_status lf_profile_enable(int enabled);
 lf_status lf_profile_collect(int kernel_id, double* total_ms, int64_t* launches);

@@ -87,8 +87,7 @@ struct StepSmem {
     static constexpr int kStageBytes = 2 * kTensorBytes;       // K + V
     static constexpr int kAgesOff = kStages * kStageBytes;
     static constexpr int kAgesBytes = kMaxChunkTiles * kTile * 4;
-    static constexpr int kListOff = kAgesOff + kAgesBytes;
-    static constexpr int kMiscOff = kListOff + kMaxChunkTiles * 4;
+    static constexpr int kMiscOff = kAgesOff + kAgesBytes;
     static constexpr int kBarOff = kMiscOff + 16;
     static constexpr int kScanBarOff = kBarOff + 2 * kStages * 8;  // the finish's 2 barriers
     static constexpr int kBytes = kScanBarOff + 16;
@@ -923,11 +922,21 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
         const int e1 = min(G * D, e0 + per);
         for (int e = e0 + tid; e < e1; e += kConsumers) {
             const int h = e / D;
+            // Every peer's value is requested before the first is used, so
+            // the remote loads share one round trip.
+            float v[kMaxClusterChunks];
+#pragma unroll
+            for (int c = 0; c < kMaxClusterChunks; ++c)
+                v[c] = (c < nchunk)
+                           ? ld_dsmem_f32(dsmem_addr(&pub_o[e], static_cast<uint32_t>(c)))
+                           : 0.f;
             float o = 0.f;
-            for (int c = 0; c < nchunk; ++c) {
-                const float w = s_w[c * G + h];
-                const float v = ld_dsmem_f32(dsmem_addr(&pub_o[e], static_cast<uint32_t>(c)));
-                o += (w != 0.f) ? w * v : 0.f;
+#pragma unroll
+            for (int c = 0; c < kMaxClusterChunks; ++c) {
+                if (c < nchunk) {
+                    const float w = s_w[c * G + h];
+                    o += (w != 0.f) ? w * v[c] : 0.f;
+                }
             }
             out[e] = __float2bfloat16_rn(o);
         }
@@ -1041,8 +1050,8 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     int32_t* ages = reinterpret_cast<int32_t*>(smem + L::kAgesOff);
-    int32_t* list = reinterpret_cast<int32_t*>(smem + L::kListOff);
-    // [0] tiles in ring order, [1] abort flag, [2] last-CTA flag, [3] live tile count
+    // [0] bit mask of the chunk's tiles that hold a live slot, [1] abort flag,
+    // [2] last-CTA flag
     volatile int32_t* misc = reinterpret_cast<int32_t*>(smem + L::kMiscOff);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
     uint64_t* empty = full + kStages;
@@ -1063,6 +1072,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
+        misc[0] = 0;
         misc[1] = 0;
         fence_barrier_init();
     }
@@ -1142,6 +1152,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     int32_t* mrow = p.mask + static_cast<size_t>(u) * S + slot0;
     const uint64_t mask_pol = l2_policy_evict_last();
     const bool ager = tid < kConsumers;
+    uint32_t live_bits = 0u;  // tiles of this thread's slots that hold a live slot
     int av[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
@@ -1167,49 +1178,40 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
                 a = na;
             }
             ages[i] = a;
+            if (a >= 0) live_bits |= 1u << (i / kTile);
         }
+    }
+    // The chunk's live tiles, gathered while ageing: one OR per warp.
+    if (ager) {
+        live_bits = __reduce_or_sync(0xffffffffu, live_bits);
+        if (lane == 0 && live_bits)
+            atomicOr(const_cast<int*>(reinterpret_cast<volatile int*>(&misc[0])),
+                     static_cast<int>(live_bits));
     }
     __syncthreads();
 
     // Tiles with no live slot are never loaded (ragged fills stream only
     // their live part), apart from speculative ones. The ring order: the
-    // nspec speculative tiles, then the other live tiles in increasing order.
-    // The live tiles, as a bit mask, tell the unit's last CTA which tiles its
-    // score scan can skip.
-    if (warp == 0) {
-        int nlist = 0;
-        int cnt = 0;
-        uint32_t bits = 0u;
-        for (int t = 0; t < ntiles; ++t) {
-            const int i0 = t * kTile + lane;
-            const int i1 = i0 + 32;
-            const bool live = __any_sync(0xffffffffu, (i0 < n && ages[i0] >= 0) || (i1 < n && ages[i1] >= 0));
-            if (live) {
-                bits |= 1u << t;
-                ++cnt;
-            }
-            if (live || t < nspec) {
-                if (lane == 0) list[nlist] = t;
-                ++nlist;
-            }
-        }
-        if (lane == 0) {
-            misc[0] = nlist;
-            misc[3] = cnt;
-            if (kScore && !kCluster && p.part_tiles && !p.split)
-                p.part_tiles[static_cast<size_t>(u) * p.nchunk + chunk] = bits;
-        }
-    }
-    __syncthreads();
-    const int nlist = misc[0];  // tiles the ring delivers
-    const int cnt = misc[3];    // tiles holding a live slot
+    // nspec speculative tiles, then the other live tiles in increasing order;
+    // the producer and the consumers walk the same bits. The live tiles, as a
+    // bit mask, also tell the unit's last CTA which tiles its score scan can
+    // skip.
+    const uint32_t live_tiles = static_cast<uint32_t>(misc[0]);
+    const uint32_t rest_tiles = live_tiles & ~((1u << nspec) - 1u);  // nspec <= kStages < 32
+    const int nlist = nspec + __popc(rest_tiles);  // tiles the ring delivers
+    const int cnt = __popc(live_tiles);            // tiles holding a live slot
+    if (kScore && !kCluster && tid == 0 && p.part_tiles && !p.split)
+        p.part_tiles[static_cast<size_t>(u) * p.nchunk + chunk] = live_tiles;
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------ producer --
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
             int issued = nspec;
+            uint32_t rest = rest_tiles;
             for (int i = nspec; i < nlist; ++i) {
+                const int t = __ffs(rest) - 1;  // the next live tile
+                rest &= rest - 1u;
                 const int s = i % kStages;
                 if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, p.wait_limit_ns)) {
                     atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
@@ -1220,7 +1222,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
                 uint8_t* kb = smem + s * L::kStageBytes;
                 uint8_t* vb = kb + L::kTensorBytes;
                 mbar_arrive_expect_tx(&full[s], L::kStageBytes);
-                const int y = slot0 + list[i] * kTile;
+                const int y = slot0 + t * kTile;
 #pragma unroll
                 for (int bx = 0; bx < L::kBoxes; ++bx) {
                     tma_load_3d(kb + bx * L::kBoxBytes, &tmK, bx * kBoxCols, y, u, &full[s], pol);
@@ -1252,8 +1254,14 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     const float sl = p.scale_log2;
     const int wrow0 = warp * 16;
 
+    uint32_t rest = rest_tiles;
     for (int i = 0; i < nlist; ++i) {
         const int s = i % kStages;
+        int t = i;  // speculative tiles first, then the live tiles in order
+        if (i >= nspec) {
+            t = __ffs(rest) - 1;
+            rest &= rest - 1u;
+        }
         if (!mbar_wait(&full[s], (i / kStages) & 1, p.wait_limit_ns)) {
             if (lane == 0) atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
             misc[1] = 1;
@@ -1261,7 +1269,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         }
         uint8_t* kb = smem + s * L::kStageBytes;
         uint8_t* vb = kb + L::kTensorBytes;
-        const int tslot0 = slot0 + list[i] * kTile;
+        const int tslot0 = slot0 + t * kTile;
 
         // Slot write, part 2: the owning warp substitutes the current token's
         // row in shared memory and stores it to the cache.

@@ -1295,24 +1295,41 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         const bool liveB = iB < n && ages[iB] >= 0;
 
         // Logits S^T and row norms ||v||_1 for this warp's 16 slots.
+        // Grids of many waves split each product into two accumulator chains
+        // (even and odd k-steps), which halves the dependent MMA chain a warp
+        // runs while it holds the ring stage (measured -0.4 to -0.8 us per
+        // step on the large batches); the latency-bound cluster grids keep
+        // one chain (measured +0.1 us with two), and so does g = 1, where
+        // two would spill at d = 128.
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
         float nv[4] = {0.f, 0.f, 0.f, 0.f};
         {
+            constexpr int kChains = (kCluster || G == 1) ? 1 : 2;
+            float sc1[4] = {0.f, 0.f, 0.f, 0.f};
+            float nv1[4] = {0.f, 0.f, 0.f, 0.f};
             const int lrow = wrow0 + (lane & 7) + ((lane >> 3) & 1) * 8;
             const uint32_t kbase = smem_u32(kb);
             const uint32_t vbase = smem_u32(vb);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
+                const bool odd = kChains == 2 && (kk & 1);
                 const uint32_t off = swz_off(lrow, 2 * kk + (lane >> 4));
                 uint32_t a[4];
                 ldsm_x4(kbase + off, a);
-                mma_bf16_16816(sc, a, qf[kk][0], qf[kk][1]);
+                mma_bf16_16816(odd ? sc1 : sc, a, qf[kk][0], qf[kk][1]);
                 if constexpr (kScore) {
                     uint32_t v[4];
                     ldsm_x4(vbase + off, v);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) v[e] &= kAbsBf16x2;
-                    mma_bf16_16816(nv, v, kOnesBf16x2, kOnesBf16x2);
+                    mma_bf16_16816(odd ? nv1 : nv, v, kOnesBf16x2, kOnesBf16x2);
+                }
+            }
+            if constexpr (kChains == 2) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    sc[e] += sc1[e];
+                    nv[e] += nv1[e];
                 }
             }
         }

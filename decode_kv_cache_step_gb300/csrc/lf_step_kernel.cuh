@@ -822,7 +822,7 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
     constexpr int kWBytes = (kConsumerWarps * G * D + 2 * kConsumerWarps * G) * 4;
     // The arrays below overlay the TMA ring, which the main loop has drained.
     static_assert(((kWBytes + 15) & ~15) +
-                          (G * D + 2 * G + 2 * kMaxClusterChunks + 3 * kMaxClusterChunks * G +
+                          (G * D + 2 * G + 2 * kMaxClusterChunks + 4 * kMaxClusterChunks * G +
                            2 * G + 2 * kConsumerWarps) * 4 <=
                       StepSmem<D, kStages>::kAgesOff,
                   "cluster epilogue arrays exceed the TMA ring");
@@ -833,7 +833,8 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
     int* pub_bestj = reinterpret_cast<int*>(pub_best + kMaxClusterChunks);   // [16]
     float2* s_mlc = reinterpret_cast<float2*>(pub_bestj + kMaxClusterChunks);  // [nchunk][G]
     float* s_w = reinterpret_cast<float*>(s_mlc + kMaxClusterChunks * G);    // [nchunk][G]
-    float* s_m = s_w + kMaxClusterChunks * G;                               // [G]
+    float* s_term = s_w + kMaxClusterChunks * G;                            // [nchunk][G]
+    float* s_m = s_term + kMaxClusterChunks * G;                            // [G]
     float* s_il = s_m + G;                                                   // [G]
     float* red_v = s_il + G;                                                 // [4]
     int* red_j = reinterpret_cast<int*>(red_v + kConsumerWarps);             // [4]
@@ -893,22 +894,30 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
         s_mlc[e] = make_float2(ld_dsmem_f32(a), ld_dsmem_f32(a + 4));
     }
     consumer_bar_sync();
-    if (tid < G) {
-        float m = NEG;
-        for (int c = 0; c < nchunk; ++c) m = fmaxf(m, s_mlc[c * G + tid].x);
-        float l = 0.f;
-        for (int c = 0; c < nchunk; ++c) {
-            const float2 v = s_mlc[c * G + tid];
-            if (v.x != NEG) l += v.y * exp2f(v.x - m);
-        }
-        s_m[tid] = m;
-        s_il[tid] = (l > 0.f) ? 1.f / l : 0.f;
+    // Thread e = (chunk c, head h) computes its own term of l_h =
+    // sum_c l_ch 2^(m_ch - m_h) (one exponential per thread, all at once),
+    // then reads the sum back; the same terms in the same order as a
+    // sequential loop over the chunks.
+    const bool ml_thread = tid < nchunk * G;  // nchunk * G <= kConsumers
+    const int h_e = tid % G;
+    float m_e = NEG, u_e = 0.f;
+    float2 v_e = make_float2(NEG, 0.f);
+    if (ml_thread) {
+        for (int c = 0; c < nchunk; ++c) m_e = fmaxf(m_e, s_mlc[c * G + h_e].x);
+        v_e = s_mlc[tid];
+        u_e = (v_e.x == NEG) ? 0.f : exp2f(v_e.x - m_e);
+        s_term[tid] = (v_e.x == NEG) ? 0.f : v_e.y * u_e;
     }
     consumer_bar_sync();
-    for (int e = tid; e < nchunk * G; e += kConsumers) {
-        const float2 v = s_mlc[e];
-        const int h = e % G;
-        s_w[e] = (v.x == NEG) ? 0.f : exp2f(v.x - s_m[h]) * s_il[h];
+    if (ml_thread) {
+        float l = 0.f;
+        for (int c = 0; c < nchunk; ++c) l += s_term[c * G + h_e];
+        const float il = (l > 0.f) ? 1.f / l : 0.f;
+        s_w[tid] = (v_e.x == NEG) ? 0.f : u_e * il;
+        if (tid < G) {
+            s_m[tid] = m_e;
+            s_il[tid] = il;
+        }
     }
     consumer_bar_sync();
 

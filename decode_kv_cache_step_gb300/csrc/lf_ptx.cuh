@@ -210,6 +210,58 @@ __device__ __forceinline__ void st_dsmem_s32(uint32_t a, int v) {
     asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
+// Split cluster barrier without memory ordering: every thread arrives once
+// and waits once. Used after mbarrier initialisation, which
+// fence_barrier_init has already released to the cluster.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait;" ::: "memory");
+}
+
+// Asynchronous 16-byte store into the shared memory of a CTA of the cluster
+// (a and bar: addresses in that CTA from dsmem_addr); the store's bytes count
+// towards the completion of that CTA's mbarrier `bar`.
+__device__ __forceinline__ void st_async_v4(uint32_t a, float x, float y, float z, float w,
+                                            uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(a),
+        "f"(x), "f"(y), "f"(z), "f"(w), "r"(bar)
+        : "memory");
+}
+
+// The same for 8 bytes (two 32-bit words).
+__device__ __forceinline__ void st_async_v2(uint32_t a, uint32_t x, uint32_t y, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.u32 [%0], {%1, %2}, [%3];" ::"r"(
+            a),
+        "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Phase wait that acquires at cluster scope: the shared-memory bytes that
+// other CTAs' asynchronous stores delivered to this barrier are visible once
+// it returns true. false after limit_ns.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // ------------------------------------------------------- warp MMA fragments --
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {

@@ -94,6 +94,53 @@ struct StepSmem {
     static constexpr int kAlloc = kBytes + 1024;               // slack for 1024-B alignment
 };
 
+// Receive buffers of the push merge (cluster grids, cluster_merge_push):
+// every consumer warp of every CTA stores its own (m, l) per head into every
+// CTA of the cluster, and each 16-row block mt of its unnormalised output
+// O^T (one float4 per lane that holds a real head pair) into CTA mt % nchunk,
+// which merges and writes those rows; rank 0 also receives every CTA's best
+// (key, slot). The bytes land through asynchronous remote stores counted on
+// an mbarrier of the receiving CTA, so no CTA reads another's shared memory
+// and no cluster barrier follows the main loop.
+template <int D, int G>
+struct PushSmem {
+    static constexpr int kPairs = (G + 1) / 2;   // head pairs (fragment columns h0, h0 + 1)
+    static constexpr int kLanes = 8 * kPairs;    // lanes of a warp holding a real head pair
+    static constexpr int kBlocks = D / 16;       // 16-row blocks of a head's output
+    // Most (source CTA, block) pairs one CTA can receive: nchunk * ceil(kBlocks / nchunk).
+    static constexpr int own_total(int n) { return n * ((kBlocks + n - 1) / n); }
+    static constexpr int own_max() {
+        int m = 0;
+        for (int n = 1; n <= kMaxClusterChunks; ++n) m = own_total(n) > m ? own_total(n) : m;
+        return m;
+    }
+    static constexpr int kParts = kMaxClusterChunks * kConsumerWarps;  // partial states, at most
+    static constexpr int kOOff = 0;  // float4 [source][own block][warp][lane]
+    static constexpr int kMlOff = kOOff + own_max() * kConsumerWarps * kLanes * 16;
+    static constexpr int kBestOff = kMlOff + kParts * kPairs * 16;    // float4 [source][warp][pair]
+    static constexpr int kWOff = kBestOff + kMaxClusterChunks * 8;     // uint2 [source]
+    static constexpr int kMOff = kWOff + kParts * G * 4;               // float [part][head]
+    static constexpr int kIlOff = kMOff + G * 4;                        // float [head]
+    static constexpr int kRedOff = kIlOff + G * 4;                      // float [head]
+    static constexpr int kBarOff = (kRedOff + 2 * kConsumerWarps * 4 + 7) & ~7;
+    static constexpr int kBytes = kBarOff + 16;  // data and best barriers
+};
+
+// Shared-memory plan of one instantiation: the cluster instances whose
+// occupancy leaves room for the push merge's receive buffers take it.
+template <int D, int G, int kStages, bool kCluster>
+struct StepAlloc {
+    using L = StepSmem<D, kStages>;
+    using P = PushSmem<D, G>;
+    static constexpr int kPushOff = (L::kBytes + 15) & ~15;
+    static constexpr int kPushAlloc = kPushOff + P::kBytes + 1024;
+    static constexpr int kPerSm = kStages == 2 ? 3 : (kStages == 3 ? 2 : 1);
+    // 227 KB per CTA at most; 228 KB per SM, 1 KB of it reserved per CTA.
+    static constexpr bool kPush =
+        kCluster && kPushAlloc <= 232448 && kPerSm * (kPushAlloc + 1024) <= 233472;
+    static constexpr int kAlloc = kPush ? kPushAlloc : L::kAlloc;
+};
+
 __device__ __forceinline__ void consumer_bar_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 }
@@ -804,6 +851,89 @@ __host__ __device__ constexpr size_t finish_smem_bytes(int nchunk, int G, int to
            (topk > 1 ? kTopKAreaBytes : 0);
 }
 
+// Score terms of the cluster epilogues' first scan batch, requested before
+// the merge so that their round trip overlaps it.
+constexpr int kScoreBatch = 8;
+
+template <int G>
+__device__ __forceinline__ void preload_terms(const StepParams& p, int u, int slot0, int n,
+                                              const int32_t* ages, int tid,
+                                              float (&t0)[kScoreBatch][G]) {
+    const float* stash0 = p.stash + (static_cast<size_t>(u) * p.S + slot0) * G;
+#pragma unroll
+    for (int k = 0; k < kScoreBatch; ++k) {
+        const int i = tid + k * kConsumers;
+        if (i < n && ages[i] >= 0) load_terms<G>(stash0 + static_cast<size_t>(i) * G, t0[k]);
+    }
+}
+
+// LongFlowScore of the chunk's slots slot0 .. slot0 + n - 1 (consumer thread
+// tid takes slots tid, tid + 128, ...) from their score terms and c_h, the
+// score export, and the thread's best candidate (key, slot): key 0xffffffff
+// and slot 0x7fffffff when it has none. t0 holds the first batch when
+// kPreloaded.
+template <int G, bool kPreloaded>
+__device__ __forceinline__ void score_chunk(const StepParams& p, int u, int slot0, int n,
+                                            const int32_t* ages, const float (&cexp)[G],
+                                            const float (&t0)[kScoreBatch][G], int tid,
+                                            uint32_t& bkey, int& bestj) {
+    const int S = p.S;
+    const float* stash = p.stash + static_cast<size_t>(u) * S * G;
+    float* scores = p.scores ? p.scores + static_cast<size_t>(u) * S : nullptr;
+    const bool fill_first = (p.flags & kFlagFillEmptyFirst) != 0;
+    const int W = p.W;
+    // A thread visits its slots in increasing order, so a strict "<" on
+    // the key (ordered_key(log2 I_j); 0 for an empty slot under
+    // fill-empty-first) keeps the lowest slot among equal keys.
+    bkey = 0xffffffffu;
+    bestj = 0x7fffffff;
+    for (int i0 = tid; i0 < n; i0 += kScoreBatch * kConsumers) {
+        float t[kScoreBatch][G];
+        if (kPreloaded && i0 == tid) {
+#pragma unroll
+            for (int k = 0; k < kScoreBatch; ++k)
+#pragma unroll
+                for (int h = 0; h < G; ++h) t[k][h] = t0[k][h];
+        } else {
+#pragma unroll
+            for (int k = 0; k < kScoreBatch; ++k) {
+                const int i = i0 + k * kConsumers;
+                if (i < n && ages[i] >= 0)
+                    load_terms<G>(stash + static_cast<size_t>(slot0 + i) * G, t[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kScoreBatch; ++k) {
+            const int i = i0 + k * kConsumers;
+            if (i >= n) break;
+            const int a = ages[i];
+            const int j = slot0 + i;
+            const float L = log2_score<G>(t[k], cexp);
+            const bool live = a >= 0;
+            const bool cand = live ? (a >= W && L == L) : fill_first;
+            const uint32_t key = live ? ordered_key(L) : 0u;
+            if (cand && key < bkey) {
+                bkey = key;
+                bestj = j;
+            }
+            if (scores) scores[j] = live ? exported_score<G>(p, L, t[k], cexp) : INFINITY;
+        }
+    }
+}
+
+// The warp's lexicographic (key, slot) minimum, in every lane.
+__device__ __forceinline__ void warp_best(uint32_t& bkey, int& bestj) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const uint32_t ok = __shfl_xor_sync(0xffffffffu, bkey, off);
+        const int oj = __shfl_xor_sync(0xffffffffu, bestj, off);
+        if (key_less(ok, oj, bkey, bestj)) {
+            bkey = ok;
+            bestj = oj;
+        }
+    }
+}
+
 // Epilogue when the unit's chunks run as one thread-block cluster (rank =
 // chunk). The chunk's merged (m, l, O) stay in shared memory; after a
 // cluster barrier every CTA reads its peers' through distributed shared
@@ -843,19 +973,11 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
     // This chunk's score terms (first batch) are requested first: they do
     // not depend on the merge, so their round trip overlaps it (the
     // consumers' barriers after the main loop ordered their stores).
-    constexpr int kBatch = 8;
     // (Held across the merge only where registers allow: the deep ring runs
     // one CTA per SM; the 2-stage ring at g = 8 would spill.)
     constexpr bool kPreload = kScore && (G <= 4 || kStages == kDeepStages);
-    float t0[kBatch][G];
-    if constexpr (kPreload) {
-        const float* stash0 = p.stash + (static_cast<size_t>(u) * p.S + slot0) * G;
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            const int i = tid + k * kConsumers;
-            if (i < n && ages[i] >= 0) load_terms<G>(stash0 + static_cast<size_t>(i) * G, t0[k]);
-        }
-    }
+    float t0[kScoreBatch][G];
+    if constexpr (kPreload) preload_terms<G>(p, u, slot0, n, ages, tid, t0);
     // This chunk's merged state, published for the cluster.
     for (int e = tid; e < G * D; e += kConsumers) {
         const int h = e / D;
@@ -956,57 +1078,11 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
         float cexp[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) cexp[h] = __log2f(s_il[h]) - s_m[h];
-        const int S = p.S;
-        const float* stash = p.stash + static_cast<size_t>(u) * S * G;
-        float* scores = p.scores ? p.scores + static_cast<size_t>(u) * S : nullptr;
-        const bool fill_first = (p.flags & kFlagFillEmptyFirst) != 0;
-        const int W = p.W;
-        // A thread visits its slots in increasing order, so a strict "<" on
-        // the key (ordered_key(log2 I_j); 0 for an empty slot under
-        // fill-empty-first) keeps the lowest slot among equal keys.
-        uint32_t bkey = 0xffffffffu;
-        int bestj = 0x7fffffff;
-        for (int i0 = tid; i0 < n; i0 += kBatch * kConsumers) {
-            float t[kBatch][G];
-            if (kPreload && i0 == tid) {
-#pragma unroll
-                for (int k = 0; k < kBatch; ++k)
-#pragma unroll
-                    for (int h = 0; h < G; ++h) t[k][h] = t0[k][h];
-            } else {
-#pragma unroll
-                for (int k = 0; k < kBatch; ++k) {
-                    const int i = i0 + k * kConsumers;
-                    if (i < n && ages[i] >= 0)
-                        load_terms<G>(stash + static_cast<size_t>(slot0 + i) * G, t[k]);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int i = i0 + k * kConsumers;
-                if (i >= n) break;
-                const int a = ages[i];
-                const int j = slot0 + i;
-                const float L = log2_score<G>(t[k], cexp);
-                const bool live = a >= 0;
-                const bool cand = live ? (a >= W && L == L) : fill_first;
-                const uint32_t key = live ? ordered_key(L) : 0u;
-                if (cand && key < bkey) {
-                    bkey = key;
-                    bestj = j;
-                }
-                if (scores) scores[j] = live ? exported_score<G>(p, L, t[k], cexp) : INFINITY;
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const uint32_t ok = __shfl_xor_sync(0xffffffffu, bkey, off);
-            const int oj = __shfl_xor_sync(0xffffffffu, bestj, off);
-            if (key_less(ok, oj, bkey, bestj)) {
-                bkey = ok;
-                bestj = oj;
-            }
-        }
+        uint32_t bkey;
+        int bestj;
+        score_chunk<G, kPreload>(p, u, slot0, n, ages, cexp, t0, tid, bkey, bestj);
+        warp_best(bkey, bestj);
+        const float* stash = p.stash + static_cast<size_t>(u) * p.S * G;
         uint32_t* red_k = reinterpret_cast<uint32_t*>(red_v);
         if ((tid & 31) == 0) {
             red_k[tid >> 5] = bkey;
@@ -1047,6 +1123,221 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
     }
 }
 
+// Merge of a cluster unit by pushes (StepAlloc::kPush). Each consumer warp
+// stores its own online-softmax state straight into the CTAs that need it
+// (PushSmem: (m, l) to all, output block mt to CTA mt % nchunk) with
+// asynchronous remote stores counted on the receiver's data barrier, and
+// arrives on its own CTA's barrier for the stores it made locally. Once a
+// CTA's barrier completes it holds the (m, l) of all 4 * nchunk partial
+// states and every partial of the output blocks it owns: it writes those
+// rows, scores its own chunk with c_h = log2(1/l_h) - m_h, and sends its
+// best (key, slot) to rank 0, which reduces the cluster's argmin. No cluster
+// barrier follows the main loop: every store into a CTA is counted on one of
+// its barriers, and a CTA leaves only after its own have completed.
+template <int D, int G, bool kScore>
+__device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, int slot0, int n,
+                                                   const int32_t* ages, uint8_t* pbase,
+                                                   const float (&acc)[D / 16][4], float m0,
+                                                   float m1, float l0, float l1, int tid) {
+    using P = PushSmem<D, G>;
+    constexpr int kPairs = P::kPairs;
+    constexpr int kLanes = P::kLanes;
+    constexpr int kBlocks = P::kBlocks;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int nchunk = p.nchunk;
+    const int rank = static_cast<int>(cluster_ctarank());
+    float4* recv_o = reinterpret_cast<float4*>(pbase + P::kOOff);
+    float4* recv_ml = reinterpret_cast<float4*>(pbase + P::kMlOff);
+    uint2* recv_best = reinterpret_cast<uint2*>(pbase + P::kBestOff);
+    float* s_w = reinterpret_cast<float*>(pbase + P::kWOff);
+    float* s_m = reinterpret_cast<float*>(pbase + P::kMOff);
+    float* s_il = reinterpret_cast<float*>(pbase + P::kIlOff);
+    uint32_t* red_k = reinterpret_cast<uint32_t*>(pbase + P::kRedOff);
+    int* red_j = reinterpret_cast<int*>(red_k + kConsumerWarps);
+    uint64_t* bar_data = reinterpret_cast<uint64_t*>(pbase + P::kBarOff);
+    uint64_t* bar_best = bar_data + 1;
+    const float NEG = -INFINITY;
+
+    // The chunk's first batch of score terms, requested before the merge
+    // (a slot's terms were stored by the warp that owns its row: the barrier
+    // orders every warp's stores before these loads).
+    float t0[kScoreBatch][G];
+    if constexpr (kScore) {
+        consumer_bar_sync();
+        preload_terms<G>(p, u, slot0, n, ages, tid, t0);
+    }
+
+    // Every CTA of the cluster has initialised its barriers (the split
+    // barrier begun at kernel start).
+    cluster_wait();
+
+    // This warp's partial state: lane (r, pair) holds heads 2 pair, 2 pair + 1
+    // of rows mt * 16 + r and + 8 of every output block, and (lanes 0 ..
+    // kPairs - 1) the pair's (m, l).
+    const int pair = lane & 3;
+    const int part = rank * kConsumerWarps + warp;
+    if (pair < kPairs) {
+        if (lane < kPairs) {
+            float4* dst = &recv_ml[part * kPairs + pair];
+            for (int c = 0; c < nchunk; ++c) {
+                if (c == rank)
+                    *dst = make_float4(m0, l0, m1, l1);
+                else
+                    st_async_v4(dsmem_addr(dst, c), m0, l0, m1, l1, dsmem_addr(bar_data, c));
+            }
+        }
+        const int vl = (lane >> 2) * kPairs + pair;
+        int c = 0, k = 0;  // owner CTA of block mt and the block's index among its own
+#pragma unroll
+        for (int mt = 0; mt < kBlocks; ++mt) {
+            const int nown = (kBlocks - c + nchunk - 1) / nchunk;
+            float4* dst = &recv_o[((rank * nown + k) * kConsumerWarps + warp) * kLanes + vl];
+            if (c == rank)
+                *dst = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+            else
+                st_async_v4(dsmem_addr(dst, c), acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3],
+                            dsmem_addr(bar_data, c));
+            if (++c == nchunk) {
+                c = 0;
+                ++k;
+            }
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_data);  // this warp's local stores
+    // The barrier completes only when every store into this CTA has landed,
+    // so it takes the full limit even under a shortened diagnostic one: the
+    // CTA must not leave while a peer's stores are in flight. (A main loop
+    // that gave up still stores its partial state, so the wait ends.)
+    if (!mbar_wait_cluster(bar_data, 0) && lane == 0) atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
+
+    // Per head (warp h): m_h over the partial states, l_h and every state's
+    // weight 2^(m_q - m_h) / l_h.
+    const int nparts = nchunk * kConsumerWarps;  // <= 64
+    for (int h = warp; h < G; h += kConsumerWarps) {
+        float2 a = make_float2(NEG, 0.f), b = make_float2(NEG, 0.f);
+        if (lane < nparts) {
+            const float4 v = recv_ml[lane * kPairs + (h >> 1)];
+            a = (h & 1) ? make_float2(v.z, v.w) : make_float2(v.x, v.y);
+        }
+        if (lane + 32 < nparts) {
+            const float4 v = recv_ml[(lane + 32) * kPairs + (h >> 1)];
+            b = (h & 1) ? make_float2(v.z, v.w) : make_float2(v.x, v.y);
+        }
+        float m = fmaxf(a.x, b.x);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        const float ea = (a.x == NEG) ? 0.f : exp2f(a.x - m);
+        const float eb = (b.x == NEG) ? 0.f : exp2f(b.x - m);
+        float l = a.y * ea + b.y * eb;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        const float il = (l > 0.f) ? 1.f / l : 0.f;
+        if (lane < nparts) s_w[lane * G + h] = ea * il;
+        if (lane + 32 < nparts) s_w[(lane + 32) * G + h] = eb * il;
+        if (lane == 0) {
+            s_m[h] = m;
+            s_il[h] = il;
+        }
+    }
+    consumer_bar_sync();
+
+    // The output rows of the blocks this CTA owns: O_h = sum_q w_qh O_qh.
+    {
+        const int b = u / p.Hkv;
+        const int kvh = u - b * p.Hkv;
+        __nv_bfloat16* out = p.out + (static_cast<size_t>(b) * p.Hq + kvh * G) * D;
+        const int nown = (kBlocks - rank + nchunk - 1) / nchunk;
+        const float* ro = reinterpret_cast<const float*>(recv_o);
+        for (int e = tid; e < nown * 16 * G; e += kConsumers) {
+            const int k = e / (16 * G);
+            const int rem = e - k * 16 * G;
+            const int h = rem >> 4;
+            const int ddl = rem & 15;
+            const int vsrc = (ddl & 7) * kPairs + (h >> 1);
+            const int comp = (h & 1) + 2 * (ddl >> 3);
+            float o = 0.f;
+            for (int c = 0; c < nchunk; ++c) {
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float wt = s_w[(c * kConsumerWarps + w) * G + h];
+                    const float v =
+                        ro[(((c * nown + k) * kConsumerWarps + w) * kLanes + vsrc) * 4 + comp];
+                    o += (wt != 0.f) ? wt * v : 0.f;
+                }
+            }
+            out[h * D + (rank + k * nchunk) * 16 + ddl] = __float2bfloat16_rn(o);
+        }
+    }
+
+    if constexpr (kScore) {
+        float cexp[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) cexp[h] = __log2f(s_il[h]) - s_m[h];
+        uint32_t bkey;
+        int bestj;
+        score_chunk<G, true>(p, u, slot0, n, ages, cexp, t0, tid, bkey, bestj);
+        warp_best(bkey, bestj);
+        if (lane == 0) {
+            red_k[warp] = bkey;
+            red_j[warp] = bestj;
+        }
+        consumer_bar_sync();
+        if (tid == 0) {
+            for (int w = 1; w < kConsumerWarps; ++w)
+                if (key_less(red_k[w], red_j[w], bkey, bestj)) {
+                    bkey = red_k[w];
+                    bestj = red_j[w];
+                }
+            if (rank != 0) {
+                st_async_v2(dsmem_addr(&recv_best[rank], 0u), bkey, static_cast<uint32_t>(bestj),
+                            dsmem_addr(bar_best, 0u));
+            } else {
+                if (nchunk > 1 && !mbar_wait_cluster(bar_best, 0))  // full limit, as above
+                    atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
+                for (int c = 1; c < nchunk; ++c) {
+                    const uint2 v = recv_best[c];
+                    if (key_less(v.x, static_cast<int>(v.y), bkey, bestj)) {
+                        bkey = v.x;
+                        bestj = static_cast<int>(v.y);
+                    }
+                }
+                const int slot = (bestj == 0x7fffffff) ? -1 : bestj;
+                p.next_slot[u] = slot;
+                if (slot >= 0 && (p.flags & kFlagMaskEvicted))
+                    p.mask[static_cast<size_t>(u) * p.S + slot] = -1;
+            }
+        }
+        // This chunk's score terms are read: drop them from L2, no write-back.
+        const float* stash = p.stash + (static_cast<size_t>(u) * p.S + slot0) * G;
+        discard_range(stash, static_cast<size_t>(n) * G * 4, tid, kConsumers);
+    }
+}
+
+// Expected bytes of a push-merge CTA's barriers, armed at kernel start: the
+// data barrier counts the remote stores of the other nchunk - 1 CTAs; rank
+// 0's best barrier their (key, slot) pairs.
+template <int D, int G, bool kScore>
+__device__ __forceinline__ void push_barriers_init(uint8_t* pbase, int nchunk) {
+    using P = PushSmem<D, G>;
+    uint64_t* bar_data = reinterpret_cast<uint64_t*>(pbase + P::kBarOff);
+    uint64_t* bar_best = bar_data + 1;
+    const int rank = static_cast<int>(cluster_ctarank());
+    mbar_init(bar_data, 1 + kConsumerWarps);
+    mbar_init(bar_best, 1);
+    const int nown = (P::kBlocks - rank + nchunk - 1) / nchunk;
+    const uint32_t per_src =
+        kConsumerWarps * (static_cast<uint32_t>(nown) * P::kLanes * 16 + P::kPairs * 16);
+    if (nchunk > 1) {
+        mbar_arrive_expect_tx(bar_data, static_cast<uint32_t>(nchunk - 1) * per_src);
+        if (kScore && rank == 0)
+            mbar_arrive_expect_tx(bar_best, static_cast<uint32_t>(nchunk - 1) * 8u);
+    } else {
+        mbar_arrive(bar_data);
+    }
+}
+
 // kStages-deep TMA ring; 3 stages run 2 CTAs per SM, 2 stages run 3.
 // kScore = false is the attention-only variant (no ageing, score or eviction).
 // kCluster: the grid is launched in clusters of nchunk CTAs (one per unit).
@@ -1055,6 +1346,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     lf_decode_step_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const StepParams p) {
     using L = StepSmem<D, kStages>;
+    using A = StepAlloc<D, G, kStages, kCluster>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1083,11 +1375,15 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         }
         misc[0] = 0;
         misc[1] = 0;
+        if constexpr (A::kPush) push_barriers_init<D, G, kScore>(smem + A::kPushOff, p.nchunk);
         fence_barrier_init();
     }
     // The barriers are initialised before any thread may use them (the
     // producer can issue copies before the prologue's barriers below).
     __syncthreads();
+    // Push merge: peers may store into this CTA once every CTA of the
+    // cluster has passed this point (waited for after the main loop).
+    if constexpr (A::kPush) cluster_arrive_relaxed();
     // With programmatic dependent launch this CTA may start while the previous
     // kernel of the stream (often the previous decode step) is still running:
     // everything above touches only this CTA's shared memory; every global
@@ -1243,7 +1539,9 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
             for (int i = max(0, issued - kStages); i < issued; ++i)
                 (void)mbar_wait(&full[i % kStages], (i / kStages) & 1);
         }
-        if constexpr (kCluster) {
+        if constexpr (A::kPush) {
+            cluster_wait();
+        } else if constexpr (kCluster) {
             __syncwarp();
             cluster_sync();  // the consumers' cluster barriers #1 and #2
             cluster_sync();
@@ -1430,6 +1728,11 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
+    if constexpr (A::kPush) {
+        cluster_merge_push<D, G, kScore>(p, u, slot0, n, ages, smem + A::kPushOff, acc, m0, m1,
+                                         l0, l1, tid);
+        return;
+    }
     consumer_bar_sync();  // every consumer is done with the stage buffers
     float* wO = reinterpret_cast<float*>(smem);  // [4][G][D]
     float* wm = wO + kConsumerWarps * G * D;     // [4][G]
@@ -1512,14 +1815,14 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
 // instances: clusters of more than 8 CTAs, an opt-in size) once per device.
 template <int D, int G, int kStages, bool kScore, bool kCluster>
 cudaError_t configure_t() {
-    using L = StepSmem<D, kStages>;
+    using A = StepAlloc<D, G, kStages, kCluster>;
     auto kernel = lf_decode_step_kernel<D, G, kStages, kScore, kCluster>;
     static int configured_for = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_for != dev) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, A::kAlloc);
         if (e != cudaSuccess) return e;
         if constexpr (kCluster) {
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -1538,7 +1841,7 @@ int max_active_clusters_t(int csize) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(csize, 1);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = StepSmem<D, kStages>::kAlloc;
+    cfg.dynamicSmemBytes = StepAlloc<D, G, kStages, true>::kAlloc;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = static_cast<unsigned>(csize);
@@ -1567,7 +1870,7 @@ int first_wave_t() {
         int per_sm = 0, sms = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                 &per_sm, lf_decode_step_kernel<D, G, kStages, kScore, false>, kThreads,
-                StepSmem<D, kStages>::kAlloc) != cudaSuccess ||
+                StepAlloc<D, G, kStages, false>::kAlloc) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
             (void)cudaGetLastError();
             return 0;
@@ -1599,7 +1902,7 @@ cudaError_t launch_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const StepP
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.nchunk, units);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.dynamicSmemBytes = StepAlloc<D, G, kStages, kCluster>::kAlloc;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int na = 0;

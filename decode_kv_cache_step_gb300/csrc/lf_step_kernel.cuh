@@ -94,36 +94,37 @@ struct StepSmem {
     static constexpr int kAlloc = kBytes + 1024;               // slack for 1024-B alignment
 };
 
-// Receive buffers of the push merge (cluster grids, cluster_merge_push):
-// every consumer warp of every CTA stores its own (m, l) per head into every
-// CTA of the cluster, and each 16-row block mt of its unnormalised output
-// O^T (one float4 per lane that holds a real head pair) into CTA mt % nchunk,
-// which merges and writes those rows; rank 0 also receives every CTA's best
-// (key, slot). The bytes land through asynchronous remote stores counted on
-// an mbarrier of the receiving CTA, so no CTA reads another's shared memory
-// and no cluster barrier follows the main loop.
+// Receive buffers of the push merge (cluster grids, cluster_merge_push).
+// Each CTA first merges its four warps' states in shared memory; then every
+// consumer thread stores one 16-byte piece of the CTA's unnormalised output
+// row (g x d floats, head-major) into the CTA that owns that piece, and the
+// CTA's (m, l) per head go to every CTA; rank 0 also receives every CTA's
+// best (key, slot). The bytes land through asynchronous remote stores
+// counted on an mbarrier of the receiving CTA, so no CTA reads another's
+// shared memory and no cluster barrier follows the main loop.
 template <int D, int G>
 struct PushSmem {
-    static constexpr int kPairs = (G + 1) / 2;   // head pairs (fragment columns h0, h0 + 1)
-    static constexpr int kLanes = 8 * kPairs;    // lanes of a warp holding a real head pair
-    static constexpr int kBlocks = D / 16;       // 16-row blocks of a head's output
-    // Most (source CTA, block) pairs one CTA can receive: nchunk * ceil(kBlocks / nchunk).
-    static constexpr int own_total(int n) { return n * ((kBlocks + n - 1) / n); }
-    static constexpr int own_max() {
+    static constexpr int kElems = G * D;  // floats of a unit's output row
+    // CTA c of nchunk owns elements [c * per, (c + 1) * per), per a multiple of 4.
+    static constexpr int per(int nchunk) { return (kElems / 4 + nchunk - 1) / nchunk * 4; }
+    static constexpr int recv_max() {
         int m = 0;
-        for (int n = 1; n <= kMaxClusterChunks; ++n) m = own_total(n) > m ? own_total(n) : m;
+        for (int n = 1; n <= kMaxClusterChunks; ++n) m = n * per(n) > m ? n * per(n) : m;
         return m;
     }
-    static constexpr int kParts = kMaxClusterChunks * kConsumerWarps;  // partial states, at most
-    static constexpr int kOOff = 0;  // float4 [source][own block][warp][lane]
-    static constexpr int kMlOff = kOOff + own_max() * kConsumerWarps * kLanes * 16;
-    static constexpr int kBestOff = kMlOff + kParts * kPairs * 16;    // float4 [source][warp][pair]
-    static constexpr int kWOff = kBestOff + kMaxClusterChunks * 8;     // uint2 [source]
-    static constexpr int kMOff = kWOff + kParts * G * 4;               // float [part][head]
+    static constexpr int kOOff = 0;                                     // float [source][per]
+    static constexpr int kMlOff = kOOff + recv_max() * 4;               // float2 [source][head]
+    static constexpr int kBestOff = kMlOff + kMaxClusterChunks * G * 8; // uint2 [source]
+    static constexpr int kWOff = kBestOff + kMaxClusterChunks * 8;      // float [source][head]
+    static constexpr int kMOff = kWOff + kMaxClusterChunks * G * 4;     // float [head]
     static constexpr int kIlOff = kMOff + G * 4;                        // float [head]
-    static constexpr int kRedOff = kIlOff + G * 4;                      // float [head]
+    static constexpr int kRedOff = kIlOff + G * 4;                      // 2 x [4 warps]
     static constexpr int kBarOff = (kRedOff + 2 * kConsumerWarps * 4 + 7) & ~7;
     static constexpr int kBytes = kBarOff + 16;  // data and best barriers
+    // The four warps' states, staged in the drained TMA ring: output rows
+    // with a padded stride (conflict-free stores), then (m, l).
+    static constexpr int kStride = D + 4;
+    static constexpr int kStageBytes = (kConsumerWarps * G * kStride + 2 * kConsumerWarps * G) * 4;
 };
 
 // Shared-memory plan of one instantiation: the cluster instances whose
@@ -1123,32 +1124,34 @@ __device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
     }
 }
 
-// Merge of a cluster unit by pushes (StepAlloc::kPush). Each consumer warp
-// stores its own online-softmax state straight into the CTAs that need it
-// (PushSmem: (m, l) to all, output block mt to CTA mt % nchunk) with
-// asynchronous remote stores counted on the receiver's data barrier, and
-// arrives on its own CTA's barrier for the stores it made locally. Once a
-// CTA's barrier completes it holds the (m, l) of all 4 * nchunk partial
-// states and every partial of the output blocks it owns: it writes those
-// rows, scores its own chunk with c_h = log2(1/l_h) - m_h, and sends its
-// best (key, slot) to rank 0, which reduces the cluster's argmin. No cluster
-// barrier follows the main loop: every store into a CTA is counted on one of
-// its barriers, and a CTA leaves only after its own have completed.
-template <int D, int G, bool kScore>
+// Merge of a cluster unit by pushes (StepAlloc::kPush). The CTA merges its
+// four warps' online-softmax states in shared memory, then each consumer
+// thread stores one 16-byte piece of the merged output row into the CTA that
+// owns it (PushSmem) and the CTA's (m, l) per head into every CTA, with
+// asynchronous remote stores counted on the receiver's data barrier; each
+// warp arrives on its own CTA's barrier for the stores it made locally. Once
+// a CTA's barrier completes it holds every chunk's (m, l) and every chunk's
+// partial of the elements it owns: it writes those, scores its own chunk
+// with c_h = log2(1/l_h) - m_h, and sends its best (key, slot) to rank 0,
+// which reduces the cluster's argmin. No cluster barrier follows the main
+// loop: every store into a CTA is counted on one of its barriers, and a CTA
+// leaves only after its own have completed.
+template <int D, int G, int kStages, bool kScore>
 __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, int slot0, int n,
-                                                   const int32_t* ages, uint8_t* pbase,
-                                                   const float (&acc)[D / 16][4], float m0,
-                                                   float m1, float l0, float l1, int tid) {
+                                                   const int32_t* ages, uint8_t* smem,
+                                                   uint8_t* pbase, const float (&acc)[D / 16][4],
+                                                   float m0, float m1, float l0, float l1,
+                                                   int tid) {
     using P = PushSmem<D, G>;
-    constexpr int kPairs = P::kPairs;
-    constexpr int kLanes = P::kLanes;
-    constexpr int kBlocks = P::kBlocks;
+    constexpr int kElems = P::kElems;
+    constexpr int kStride = P::kStride;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int nchunk = p.nchunk;
     const int rank = static_cast<int>(cluster_ctarank());
-    float4* recv_o = reinterpret_cast<float4*>(pbase + P::kOOff);
-    float4* recv_ml = reinterpret_cast<float4*>(pbase + P::kMlOff);
+    const int per = P::per(nchunk);
+    float* recv_o = reinterpret_cast<float*>(pbase + P::kOOff);
+    float2* recv_ml = reinterpret_cast<float2*>(pbase + P::kMlOff);
     uint2* recv_best = reinterpret_cast<uint2*>(pbase + P::kBestOff);
     float* s_w = reinterpret_cast<float*>(pbase + P::kWOff);
     float* s_m = reinterpret_cast<float*>(pbase + P::kMOff);
@@ -1157,52 +1160,96 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
     int* red_j = reinterpret_cast<int*>(red_k + kConsumerWarps);
     uint64_t* bar_data = reinterpret_cast<uint64_t*>(pbase + P::kBarOff);
     uint64_t* bar_best = bar_data + 1;
+    float* wO = reinterpret_cast<float*>(smem);            // [4][G][kStride]
+    float* wm = wO + kConsumerWarps * G * kStride;          // [4][G]
+    float* wl = wm + kConsumerWarps * G;                    // [4][G]
     const float NEG = -INFINITY;
 
+    // Every warp is done with the ring, and every slot's score terms (stored
+    // by the warp that owns its row) are ordered before the loads below.
+    consumer_bar_sync();
     // The chunk's first batch of score terms, requested before the merge
-    // (a slot's terms were stored by the warp that owns its row: the barrier
-    // orders every warp's stores before these loads).
+    // (held across it only where registers allow, as in cluster_epilogue).
+    constexpr bool kPreload = kScore && (G <= 4 || kStages == kDeepStages);
     float t0[kScoreBatch][G];
-    if constexpr (kScore) {
-        consumer_bar_sync();
-        preload_terms<G>(p, u, slot0, n, ages, tid, t0);
+    if constexpr (kPreload) preload_terms<G>(p, u, slot0, n, ages, tid, t0);
+
+    // The four warps' states: lane (r, pair) holds heads h0 = 2 pair, h0 + 1
+    // of rows mt * 16 + r and + 8 of every 16-row block.
+    {
+        const int r = lane >> 2;
+        const int h0 = 2 * (lane & 3);
+        if (r == 0) {
+            if (h0 < G) { wm[warp * G + h0] = m0; wl[warp * G + h0] = l0; }
+            if (h0 + 1 < G) { wm[warp * G + h0 + 1] = m1; wl[warp * G + h0 + 1] = l1; }
+        }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            const int dd = mt * 16 + r;
+            if (h0 < G) {
+                wO[(warp * G + h0) * kStride + dd] = acc[mt][0];
+                wO[(warp * G + h0) * kStride + dd + 8] = acc[mt][2];
+            }
+            if (h0 + 1 < G) {
+                wO[(warp * G + h0 + 1) * kStride + dd] = acc[mt][1];
+                wO[(warp * G + h0 + 1) * kStride + dd + 8] = acc[mt][3];
+            }
+        }
     }
+    consumer_bar_sync();
 
     // Every CTA of the cluster has initialised its barriers (the split
     // barrier begun at kernel start).
     cluster_wait();
 
-    // This warp's partial state: lane (r, pair) holds heads 2 pair, 2 pair + 1
-    // of rows mt * 16 + r and + 8 of every output block, and (lanes 0 ..
-    // kPairs - 1) the pair's (m, l).
-    const int pair = lane & 3;
-    const int part = rank * kConsumerWarps + warp;
-    if (pair < kPairs) {
-        if (lane < kPairs) {
-            float4* dst = &recv_ml[part * kPairs + pair];
-            for (int c = 0; c < nchunk; ++c) {
-                if (c == rank)
-                    *dst = make_float4(m0, l0, m1, l1);
-                else
-                    st_async_v4(dsmem_addr(dst, c), m0, l0, m1, l1, dsmem_addr(bar_data, c));
-            }
-        }
-        const int vl = (lane >> 2) * kPairs + pair;
-        int c = 0, k = 0;  // owner CTA of block mt and the block's index among its own
+    // The CTA's merged output row, 4 elements per thread, each piece to the
+    // CTA that owns it; then (m, l) of head h to CTA c (thread c * G + h).
+    for (int e = 4 * tid; e < kElems; e += 4 * kConsumers) {
+        const int h = e / D;
+        const int d = e - h * D;
+        float mw[kConsumerWarps];
+        float mh = NEG;
 #pragma unroll
-        for (int mt = 0; mt < kBlocks; ++mt) {
-            const int nown = (kBlocks - c + nchunk - 1) / nchunk;
-            float4* dst = &recv_o[((rank * nown + k) * kConsumerWarps + warp) * kLanes + vl];
-            if (c == rank)
-                *dst = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
-            else
-                st_async_v4(dsmem_addr(dst, c), acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3],
-                            dsmem_addr(bar_data, c));
-            if (++c == nchunk) {
-                c = 0;
-                ++k;
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            mw[w] = wm[w * G + h];
+            mh = fmaxf(mh, mw[w]);
+        }
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            if (mw[w] != NEG) {
+                const float ew = exp2f(mw[w] - mh);
+                const float4 v = *reinterpret_cast<const float4*>(&wO[(w * G + h) * kStride + d]);
+                o.x += v.x * ew;
+                o.y += v.y * ew;
+                o.z += v.z * ew;
+                o.w += v.w * ew;
             }
         }
+        const int c = e / per;
+        float* dst = &recv_o[rank * per + (e - c * per)];
+        if (c == rank)
+            *reinterpret_cast<float4*>(dst) = o;
+        else
+            st_async_v4(dsmem_addr(dst, c), o.x, o.y, o.z, o.w, dsmem_addr(bar_data, c));
+    }
+    if (tid < nchunk * G) {
+        const int c = tid / G;
+        const int h = tid - c * G;
+        float mh = NEG, l = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) mh = fmaxf(mh, wm[w * G + h]);
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float mw = wm[w * G + h];
+            if (mw != NEG) l += wl[w * G + h] * exp2f(mw - mh);
+        }
+        float2* dst = &recv_ml[rank * G + h];
+        if (c == rank)
+            *dst = make_float2(mh, l);
+        else
+            st_async_v2(dsmem_addr(dst, c), __float_as_uint(mh), __float_as_uint(l),
+                        dsmem_addr(bar_data, c));
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_data);  // this warp's local stores
@@ -1212,30 +1259,19 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
     // that gave up still stores its partial state, so the wait ends.)
     if (!mbar_wait_cluster(bar_data, 0) && lane == 0) atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
 
-    // Per head (warp h): m_h over the partial states, l_h and every state's
-    // weight 2^(m_q - m_h) / l_h.
-    const int nparts = nchunk * kConsumerWarps;  // <= 64
+    // Per head (warp h): m_h over the chunks, l_h and every chunk's weight
+    // 2^(m_c - m_h) / l_h.
     for (int h = warp; h < G; h += kConsumerWarps) {
-        float2 a = make_float2(NEG, 0.f), b = make_float2(NEG, 0.f);
-        if (lane < nparts) {
-            const float4 v = recv_ml[lane * kPairs + (h >> 1)];
-            a = (h & 1) ? make_float2(v.z, v.w) : make_float2(v.x, v.y);
-        }
-        if (lane + 32 < nparts) {
-            const float4 v = recv_ml[(lane + 32) * kPairs + (h >> 1)];
-            b = (h & 1) ? make_float2(v.z, v.w) : make_float2(v.x, v.y);
-        }
-        float m = fmaxf(a.x, b.x);
+        const float2 a = (lane < nchunk) ? recv_ml[lane * G + h] : make_float2(NEG, 0.f);
+        float m = a.x;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
         const float ea = (a.x == NEG) ? 0.f : exp2f(a.x - m);
-        const float eb = (b.x == NEG) ? 0.f : exp2f(b.x - m);
-        float l = a.y * ea + b.y * eb;
+        float l = a.y * ea;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        for (int off = 8; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
         const float il = (l > 0.f) ? 1.f / l : 0.f;
-        if (lane < nparts) s_w[lane * G + h] = ea * il;
-        if (lane + 32 < nparts) s_w[(lane + 32) * G + h] = eb * il;
+        if (lane < nchunk) s_w[lane * G + h] = ea * il;
         if (lane == 0) {
             s_m[h] = m;
             s_il[h] = il;
@@ -1243,31 +1279,21 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
     }
     consumer_bar_sync();
 
-    // The output rows of the blocks this CTA owns: O_h = sum_q w_qh O_qh.
+    // The output elements this CTA owns: O_h = sum_c w_ch O_ch.
     {
         const int b = u / p.Hkv;
         const int kvh = u - b * p.Hkv;
         __nv_bfloat16* out = p.out + (static_cast<size_t>(b) * p.Hq + kvh * G) * D;
-        const int nown = (kBlocks - rank + nchunk - 1) / nchunk;
-        const float* ro = reinterpret_cast<const float*>(recv_o);
-        for (int e = tid; e < nown * 16 * G; e += kConsumers) {
-            const int k = e / (16 * G);
-            const int rem = e - k * 16 * G;
-            const int h = rem >> 4;
-            const int ddl = rem & 15;
-            const int vsrc = (ddl & 7) * kPairs + (h >> 1);
-            const int comp = (h & 1) + 2 * (ddl >> 3);
+        const int e0 = rank * per;
+        const int cnt = min(per, kElems - e0);
+        for (int e = tid; e < cnt; e += kConsumers) {
+            const int h = (e0 + e) / D;
             float o = 0.f;
             for (int c = 0; c < nchunk; ++c) {
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float wt = s_w[(c * kConsumerWarps + w) * G + h];
-                    const float v =
-                        ro[(((c * nown + k) * kConsumerWarps + w) * kLanes + vsrc) * 4 + comp];
-                    o += (wt != 0.f) ? wt * v : 0.f;
-                }
+                const float wt = s_w[c * G + h];
+                o += (wt != 0.f) ? wt * recv_o[c * per + e] : 0.f;
             }
-            out[h * D + (rank + k * nchunk) * 16 + ddl] = __float2bfloat16_rn(o);
+            out[e0 + e] = __float2bfloat16_rn(o);
         }
     }
 
@@ -1277,7 +1303,7 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
         for (int h = 0; h < G; ++h) cexp[h] = __log2f(s_il[h]) - s_m[h];
         uint32_t bkey;
         int bestj;
-        score_chunk<G, true>(p, u, slot0, n, ages, cexp, t0, tid, bkey, bestj);
+        score_chunk<G, kPreload>(p, u, slot0, n, ages, cexp, t0, tid, bkey, bestj);
         warp_best(bkey, bestj);
         if (lane == 0) {
             red_k[warp] = bkey;
@@ -1316,8 +1342,9 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
 }
 
 // Expected bytes of a push-merge CTA's barriers, armed at kernel start: the
-// data barrier counts the remote stores of the other nchunk - 1 CTAs; rank
-// 0's best barrier their (key, slot) pairs.
+// data barrier counts the remote stores of the other nchunk - 1 CTAs (the
+// elements this CTA owns and (m, l) per head from each); rank 0's best
+// barrier their (key, slot) pairs.
 template <int D, int G, bool kScore>
 __device__ __forceinline__ void push_barriers_init(uint8_t* pbase, int nchunk) {
     using P = PushSmem<D, G>;
@@ -1326,9 +1353,9 @@ __device__ __forceinline__ void push_barriers_init(uint8_t* pbase, int nchunk) {
     const int rank = static_cast<int>(cluster_ctarank());
     mbar_init(bar_data, 1 + kConsumerWarps);
     mbar_init(bar_best, 1);
-    const int nown = (P::kBlocks - rank + nchunk - 1) / nchunk;
-    const uint32_t per_src =
-        kConsumerWarps * (static_cast<uint32_t>(nown) * P::kLanes * 16 + P::kPairs * 16);
+    const int per = P::per(nchunk);
+    const int own = max(0, min(per, P::kElems - rank * per));
+    const uint32_t per_src = static_cast<uint32_t>(own) * 4u + G * 8u;
     if (nchunk > 1) {
         mbar_arrive_expect_tx(bar_data, static_cast<uint32_t>(nchunk - 1) * per_src);
         if (kScore && rank == 0)
@@ -1729,8 +1756,9 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
     if constexpr (A::kPush) {
-        cluster_merge_push<D, G, kScore>(p, u, slot0, n, ages, smem + A::kPushOff, acc, m0, m1,
-                                         l0, l1, tid);
+        static_assert(PushSmem<D, G>::kStageBytes <= L::kAgesOff, "warp states exceed the TMA ring");
+        cluster_merge_push<D, G, kStages, kScore>(p, u, slot0, n, ages, smem, smem + A::kPushOff,
+                                                  acc, m0, m1, l0, l1, tid);
         return;
     }
     consumer_bar_sync();  // every consumer is done with the stage buffers

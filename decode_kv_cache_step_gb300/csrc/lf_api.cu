@@ -263,13 +263,9 @@ struct Plan {
 // Units of at least this many slots take the split finish.
 constexpr int kSplitMinSlots = 8192;
 
-// Largest cluster by default: 16 CTAs, a non-portable size (measured: the
-// 3200-slot Qwen3 shape at batch 2 and 4 runs 14.4 and 14.6 us per step in
-// clusters of up to 16 against 15.3 and 16.2 in clusters of up to 8; one
-// sequence and the 2400-slot ragged batches unchanged). Where clusters of
-// that size cannot be placed the plan falls back to 8.
+// Largest cluster the plan tries by default: 16 CTAs, a non-portable size
+// (smaller ones are tried where it cannot be placed).
 constexpr int kDefaultClusterChunks = 16;
-constexpr int kPortableClusterChunks = 8;
 
 // Split the slot axis of every unit into nchunk chunks of chunk_tiles tiles.
 // Each CTA costs a fixed start-up and merge, so chunks stay long (13 to 32
@@ -310,11 +306,26 @@ Plan plan_split(int S, int units, int sms, bool want_cluster, int D, int G, bool
     // resident at once merges inside thread-block clusters: the
     // latency-bound small batches gain the shorter merge. Larger grids keep
     // the last-CTA merge, where a finished CTA frees its slot at once instead
-    // of waiting for its cluster. LF_CLUSTER=0 turns clusters off, =1 forces
-    // them whenever the shape allows. A cluster must sit within one GPC, so
-    // how many fit at once comes from the occupancy query, not the SM count
+    // of waiting for its cluster. A cluster must sit within one GPC, so how
+    // many fit at once comes from the occupancy query, not the SM count
     // (measured: 16 clusters of 8 one-per-SM CTAs, 128 of 152 SMs, took two
     // waves: 21.6 us per step against 10.4 for one cluster).
+    // A step of such a grid is a chain of round trips that shortens with the
+    // chunk, so among the splits whose clusters all fit the plan takes, for
+    // each TMA ring, the one with the most chunks: the 2-stage ring at three
+    // CTAs per SM, and the kDeepStages ring at one CTA per SM, which keeps
+    // every tile of a short chunk in flight. Of the two it takes the shorter
+    // modelled chain, about 0.55 us per tile of chunk on the deep ring and
+    // 0.9 us per tile plus 0.9 on the 2-stage ring. Measured per step: one
+    // 2400-slot Qwen3 sequence 7.7 us in 10 chunks of 4 tiles on the deep
+    // ring, 9.1 in 13 of 3 on the 2-stage ring, 8.4 in 8 of 5 on the deep
+    // ring; two ragged 2400-slot sequences 9.6 us in 13 of 3 on the 2-stage
+    // ring against 10.3 in 5 of 8 on the deep ring; the 3200-slot Qwen3 shape
+    // at batch 8, 6 chunks of 9 tiles in clusters 20.2 us against 30.8 for
+    // the last-CTA merge over 10 of 5.
+    // LF_CLUSTER=0 turns clusters off, =1 forces them whenever one cluster of
+    // the split can be placed; LF_DEEP=0 keeps the 2-stage ring, =1 takes the
+    // deep ring whenever its clusters all fit.
     pl.cluster = false;
     const char* cenv = std::getenv("LF_CLUSTER");
     const int cmode = cenv ? std::atoi(cenv) : -1;
@@ -324,58 +335,48 @@ Plan plan_split(int S, int units, int sms, bool want_cluster, int D, int G, bool
     const char* denv = std::getenv("LF_DEEP");
     const int dmode = denv ? std::atoi(denv) : -1;
     pl.fit = -1;
-    bool first = true;
-    for (int cap : {cmax, std::min(cmax, kPortableClusterChunks)}) {
-        if (!want_cluster || pl.stages != 2 || cmode == 0 || pl.tiles > cap * lf::kMaxChunkTiles)
-            break;
-        int ct = pl.chunk_tiles, nc = pl.nchunk;
-        if (nc > cap) {
-            ct = (pl.tiles + cap - 1) / cap;
-            nc = (pl.tiles + ct - 1) / ct;
-        }
-        int fit = lf::max_active_clusters(D, G, 2, score, nc);
-        if (first) pl.fit = fit;
-        first = false;
-        if (fit == 0 && nc > kPortableClusterChunks) continue;  // this size cannot be placed
-        if (fit > 0 && units > fit && cmode != 1 && !forced_chunks) {
-            // Too many units for clusters of nc: take the largest smaller
-            // cluster (longer chunks, at most kMaxChunkTiles tiles) whose
-            // clusters are all resident at once. Measured against the
-            // last-CTA plan: the 3200-slot Qwen3 shape at batch 8, 6 chunks of
-            // 9 tiles in clusters 22.4 us per step against 29.9 for 10 of 5;
-            // at batch 16, 3 of 17 in clusters 38.2 against 50.1 for 4 of 13;
-            // four 16K-slot sequences, 12 of 22 in clusters 45.6 against 58.7
-            // for 20 of 13 with the split finish.
-            for (int n2 = nc - 1; n2 >= 1; --n2) {
-                const int ct2 = (pl.tiles + n2 - 1) / n2;
-                if (ct2 > lf::kMaxChunkTiles) break;
-                const int nc2 = (pl.tiles + ct2 - 1) / ct2;
-                const int f2 = lf::max_active_clusters(D, G, 2, score, nc2);
-                if (units <= f2) {
-                    ct = ct2;
-                    nc = nc2;
-                    fit = f2;
-                    break;
+    if (want_cluster && pl.stages == 2 && cmode != 0 && pl.tiles <= cmax * lf::kMaxChunkTiles) {
+        struct Split {
+            int ct = 0, nc = 0, fit = 0;
+        };
+        Split two, deep, first;
+        // Splits by decreasing chunk count; a forced split (LF_CHUNK_TILES)
+        // is the only one tried.
+        const int n_hi = forced_chunks ? pl.nchunk : std::min(cmax, pl.tiles);
+        for (int n0 = n_hi; n0 >= 1; --n0) {
+            const int ct = (pl.tiles + n0 - 1) / n0;
+            if (ct > lf::kMaxChunkTiles) break;
+            const int nc = (pl.tiles + ct - 1) / ct;
+            if (nc != n0) continue;  // the same split as a larger n0
+            if (nc <= cmax) {
+                const int f2 = lf::max_active_clusters(D, G, 2, score, nc);
+                if (first.nc == 0) first = {ct, nc, f2};
+                if (two.nc == 0 && units <= f2) two = {ct, nc, f2};
+                if (dmode != 0 && deep.nc == 0) {
+                    const int fd = lf::max_active_clusters(D, G, lf::kDeepStages, score, nc);
+                    if (units <= fd) deep = {ct, nc, fd};
                 }
             }
+            if (forced_chunks || (two.nc != 0 && (deep.nc != 0 || dmode == 0))) break;
         }
-        if (fit > 0 && (cmode == 1 || units <= fit)) {
-            pl.chunk_tiles = ct;
-            pl.nchunk = nc;
+        Split pick;
+        bool take_deep = false;
+        if (deep.nc != 0 && (dmode == 1 || two.nc == 0 || 55 * deep.ct <= 90 * two.ct + 90)) {
+            pick = deep;
+            take_deep = true;
+        } else if (two.nc != 0) {
+            pick = two;
+        } else if (cmode == 1 && first.fit > 0) {
+            pick = first;  // forced: clusters in more than one wave
+        }
+        pl.fit = first.fit;
+        if (pick.nc != 0) {
+            pl.chunk_tiles = pick.ct;
+            pl.nchunk = pick.nc;
             pl.cluster = true;
-            pl.fit = fit;
-            // Clusters of one CTA per SM, all resident at once, have room
-            // for a deep TMA ring: every tile of a short chunk is in flight
-            // at once, which shortens the chain of round trips of a
-            // latency-bound step. It pays from 5 tiles per chunk (3 turns of
-            // a 2-stage ring; measured: one 2400-slot sequence 12.5 -> 11.5
-            // us per step, a 4-tile chunk no gain). LF_DEEP=0: off;
-            // LF_DEEP=1: also for shorter chunks.
-            if (dmode != 0 && (dmode == 1 || ct >= 5) &&
-                units <= lf::max_active_clusters(D, G, lf::kDeepStages, score, nc))
-                pl.stages = lf::kDeepStages;
+            pl.fit = pick.fit;
+            if (take_deep) pl.stages = lf::kDeepStages;
         }
-        break;
     }
     // Top-1 steps over long units without clusters score in a second kernel:
     // the last CTA's scan of every slot would otherwise run on the step's

@@ -176,38 +176,11 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
-// All threads of the cluster: release this CTA's shared-memory writes and
-// acquire every other CTA's (hardware barrier; every CTA of a cluster is
-// resident together).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
 // Address of this CTA's shared variable `p` in the CTA of cluster rank `rank`.
 __device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
     uint32_t a;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
     return a;
-}
-
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ int ld_dsmem_s32(uint32_t a) {
-    int v;
-    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_dsmem_f32(uint32_t a, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_dsmem_s32(uint32_t a, int v) {
-    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
 // Split cluster barrier without memory ordering: every thread arrives once

@@ -48,11 +48,13 @@
 // the step's memory traffic is over. Shorter ragged units scan only the tiles
 // that hold a live slot (top-1; the chunk CTAs publish their live-tile
 // masks). When every unit's cluster (up to 16 CTAs) can be resident at once,
-// a unit's chunks run as one thread-block cluster instead (kCluster): they
-// merge through distributed shared memory and each CTA scores its own chunk
-// (top-1 only). A cluster
-// grid of at most one CTA per SM uses a kDeepStages-deep TMA ring, so every
-// tile of a short chunk is in flight at once.
+// a unit's chunks run as one thread-block cluster instead (kCluster): the
+// CTAs push their merged states into one another's shared memory with
+// asynchronous remote stores counted on mbarriers (cluster_merge_push), each
+// writes the part of the output row it owns and scores its own chunk, and
+// rank 0 reduces the argmin (top-1 only). A cluster grid of at most one CTA
+// per SM uses a kDeepStages-deep TMA ring, so every tile of a short chunk is
+// in flight at once.
 // An attention-only instantiation (kScore = false) drops the row norms, the
 // score terms, the ageing and the selection: the baseline for the overhead.
 // Launches use programmatic dependent launch: a CTA lets the next kernel of
@@ -65,6 +67,7 @@
 #include <stdlib.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "../../include/lf_decode.h"
 #include "lf_kernels.h"
@@ -78,16 +81,34 @@ constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr uint32_t kOnesBf16x2 = 0x3F803F80u;   // (1.0, 1.0) in bf16
 constexpr uint32_t kAbsBf16x2 = 0x7FFF7FFFu;
+constexpr int kSlotLive = 1;  // slot flag: age >= 0 after the step's ageing
+constexpr int kSlotOld = 2;   // slot flag: age >= W (may be evicted)
 
-template <int D, int kStages>
+// The chunk's per-slot state in shared memory: cluster instances keep the
+// two flags in a byte; the others keep the age itself (measured: flag bytes
+// cost the last-CTA instances 0.5% on the full batches).
+template <bool kCluster>
+using SlotState = typename std::conditional<kCluster, uint8_t, int32_t>::type;
+
+__device__ __forceinline__ uint8_t slot_state(int a, int W, uint8_t*) {
+    return static_cast<uint8_t>((a >= 0 ? kSlotLive : 0) | (a >= W ? kSlotOld : 0));
+}
+__device__ __forceinline__ int32_t slot_state(int a, int, int32_t*) { return a; }
+__device__ __forceinline__ bool slot_live(uint8_t f) { return (f & kSlotLive) != 0; }
+__device__ __forceinline__ bool slot_live(int32_t a) { return a >= 0; }
+
+// Shared memory of one CTA: the TMA ring, the chunk's slot states
+// (SlotState: a flag byte per slot in cluster instances, the age in the
+// others), misc words and barriers.
+template <int D, int kStages, bool kCluster = false>
 struct StepSmem {
     static constexpr int kBoxes = D / kBoxCols;
     static constexpr int kBoxBytes = kTile * 128;              // 64 rows x 128 B
     static constexpr int kTensorBytes = kBoxes * kBoxBytes;    // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kTensorBytes;       // K + V
-    static constexpr int kAgesOff = kStages * kStageBytes;
-    static constexpr int kAgesBytes = kMaxChunkTiles * kTile * 4;
-    static constexpr int kMiscOff = kAgesOff + kAgesBytes;
+    static constexpr int kFlagsOff = kStages * kStageBytes;
+    static constexpr int kFlagsBytes = kMaxChunkTiles * kTile * (kCluster ? 1 : 4);
+    static constexpr int kMiscOff = kFlagsOff + kFlagsBytes;
     static constexpr int kBarOff = kMiscOff + 16;
     static constexpr int kScanBarOff = kBarOff + 2 * kStages * 8;  // the finish's 2 barriers
     static constexpr int kBytes = kScanBarOff + 16;
@@ -120,18 +141,18 @@ struct PushSmem {
     static constexpr int kIlOff = kMOff + G * 4;                        // float [head]
     static constexpr int kRedOff = kIlOff + G * 4;                      // 2 x [4 warps]
     static constexpr int kBarOff = (kRedOff + 2 * kConsumerWarps * 4 + 7) & ~7;
-    static constexpr int kBytes = kBarOff + 16;  // data and best barriers
+    static constexpr int kBytes = kBarOff + 24;  // (m, l), output and best barriers
     // The four warps' states, staged in the drained TMA ring: output rows
     // with a padded stride (conflict-free stores), then (m, l).
     static constexpr int kStride = D + 4;
     static constexpr int kStageBytes = (kConsumerWarps * G * kStride + 2 * kConsumerWarps * G) * 4;
 };
 
-// Shared-memory plan of one instantiation: the cluster instances whose
-// occupancy leaves room for the push merge's receive buffers take it.
+// Shared-memory plan of one instantiation: cluster instances add the push
+// merge's receive buffers (kPush: they fit at the instance's occupancy).
 template <int D, int G, int kStages, bool kCluster>
 struct StepAlloc {
-    using L = StepSmem<D, kStages>;
+    using L = StepSmem<D, kStages, kCluster>;
     using P = PushSmem<D, G>;
     static constexpr int kPushOff = (L::kBytes + 15) & ~15;
     static constexpr int kPushAlloc = kPushOff + P::kBytes + 1024;
@@ -858,13 +879,14 @@ constexpr int kScoreBatch = 8;
 
 template <int G>
 __device__ __forceinline__ void preload_terms(const StepParams& p, int u, int slot0, int n,
-                                              const int32_t* ages, int tid,
+                                              const uint8_t* sflags, int tid,
                                               float (&t0)[kScoreBatch][G]) {
     const float* stash0 = p.stash + (static_cast<size_t>(u) * p.S + slot0) * G;
 #pragma unroll
     for (int k = 0; k < kScoreBatch; ++k) {
         const int i = tid + k * kConsumers;
-        if (i < n && ages[i] >= 0) load_terms<G>(stash0 + static_cast<size_t>(i) * G, t0[k]);
+        if (i < n && (sflags[i] & kSlotLive))
+            load_terms<G>(stash0 + static_cast<size_t>(i) * G, t0[k]);
     }
 }
 
@@ -875,14 +897,13 @@ __device__ __forceinline__ void preload_terms(const StepParams& p, int u, int sl
 // kPreloaded.
 template <int G, bool kPreloaded>
 __device__ __forceinline__ void score_chunk(const StepParams& p, int u, int slot0, int n,
-                                            const int32_t* ages, const float (&cexp)[G],
+                                            const uint8_t* sflags, const float (&cexp)[G],
                                             const float (&t0)[kScoreBatch][G], int tid,
                                             uint32_t& bkey, int& bestj) {
     const int S = p.S;
     const float* stash = p.stash + static_cast<size_t>(u) * S * G;
     float* scores = p.scores ? p.scores + static_cast<size_t>(u) * S : nullptr;
     const bool fill_first = (p.flags & kFlagFillEmptyFirst) != 0;
-    const int W = p.W;
     // A thread visits its slots in increasing order, so a strict "<" on
     // the key (ordered_key(log2 I_j); 0 for an empty slot under
     // fill-empty-first) keeps the lowest slot among equal keys.
@@ -899,7 +920,7 @@ __device__ __forceinline__ void score_chunk(const StepParams& p, int u, int slot
 #pragma unroll
             for (int k = 0; k < kScoreBatch; ++k) {
                 const int i = i0 + k * kConsumers;
-                if (i < n && ages[i] >= 0)
+                if (i < n && (sflags[i] & kSlotLive))
                     load_terms<G>(stash + static_cast<size_t>(slot0 + i) * G, t[k]);
             }
         }
@@ -907,11 +928,11 @@ __device__ __forceinline__ void score_chunk(const StepParams& p, int u, int slot
         for (int k = 0; k < kScoreBatch; ++k) {
             const int i = i0 + k * kConsumers;
             if (i >= n) break;
-            const int a = ages[i];
+            const int f = sflags[i];
             const int j = slot0 + i;
             const float L = log2_score<G>(t[k], cexp);
-            const bool live = a >= 0;
-            const bool cand = live ? (a >= W && L == L) : fill_first;
+            const bool live = (f & kSlotLive) != 0;
+            const bool cand = live ? ((f & kSlotOld) && L == L) : fill_first;
             const uint32_t key = live ? ordered_key(L) : 0u;
             if (cand && key < bkey) {
                 bkey = key;
@@ -935,210 +956,21 @@ __device__ __forceinline__ void warp_best(uint32_t& bkey, int& bestj) {
     }
 }
 
-// Epilogue when the unit's chunks run as one thread-block cluster (rank =
-// chunk). The chunk's merged (m, l, O) stay in shared memory; after a
-// cluster barrier every CTA reads its peers' through distributed shared
-// memory. CTA r writes its slice of the output row, every CTA scores only
-// its own chunk's slots and writes its local best into rank 0's shared
-// memory, and rank 0 reduces the cluster's (I_j, j) argmin after the second
-// (last) cluster barrier. wO/wm/wl hold the four consumer warps' states
-// (consumer threads only; the producer warp joins the two cluster barriers
-// on its own).
-template <int D, int G, int kStages, bool kScore>
-__device__ void cluster_epilogue(const StepParams& p, int u, int slot0, int n,
-                                 const int32_t* ages, uint8_t* smem, const float* wO,
-                                 const float* wm, const float* wl, int cnt, int tid) {
-    const int nchunk = p.nchunk;
-    const uint32_t rank = cluster_ctarank();
-    constexpr int kWBytes = (kConsumerWarps * G * D + 2 * kConsumerWarps * G) * 4;
-    // The arrays below overlay the TMA ring, which the main loop has drained.
-    static_assert(((kWBytes + 15) & ~15) +
-                          (G * D + 2 * G + 2 * kMaxClusterChunks + 4 * kMaxClusterChunks * G +
-                           2 * G + 2 * kConsumerWarps) * 4 <=
-                      StepSmem<D, kStages>::kAgesOff,
-                  "cluster epilogue arrays exceed the TMA ring");
-    float* pub_o = reinterpret_cast<float*>(smem + ((kWBytes + 15) & ~15));  // [G][D]
-    float2* pub_ml = reinterpret_cast<float2*>(pub_o + G * D);               // [G]
-    // Every CTA's local best (key, slot), written into rank 0's copy of these arrays.
-    uint32_t* pub_best = reinterpret_cast<uint32_t*>(pub_ml + G);            // [16]
-    int* pub_bestj = reinterpret_cast<int*>(pub_best + kMaxClusterChunks);   // [16]
-    float2* s_mlc = reinterpret_cast<float2*>(pub_bestj + kMaxClusterChunks);  // [nchunk][G]
-    float* s_w = reinterpret_cast<float*>(s_mlc + kMaxClusterChunks * G);    // [nchunk][G]
-    float* s_term = s_w + kMaxClusterChunks * G;                            // [nchunk][G]
-    float* s_m = s_term + kMaxClusterChunks * G;                            // [G]
-    float* s_il = s_m + G;                                                   // [G]
-    float* red_v = s_il + G;                                                 // [4]
-    int* red_j = reinterpret_cast<int*>(red_v + kConsumerWarps);             // [4]
-    const float NEG = -INFINITY;
-
-    // This chunk's score terms (first batch) are requested first: they do
-    // not depend on the merge, so their round trip overlaps it (the
-    // consumers' barriers after the main loop ordered their stores).
-    // (Held across the merge only where registers allow: the deep ring runs
-    // one CTA per SM; the 2-stage ring at g = 8 would spill.)
-    constexpr bool kPreload = kScore && (G <= 4 || kStages == kDeepStages);
-    float t0[kScoreBatch][G];
-    if constexpr (kPreload) preload_terms<G>(p, u, slot0, n, ages, tid, t0);
-    // This chunk's merged state, published for the cluster.
-    for (int e = tid; e < G * D; e += kConsumers) {
-        const int h = e / D;
-        float mh = NEG;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) mh = fmaxf(mh, wm[w * G + h]);
-        float o = 0.f;
-        if (cnt > 0) {
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float mw = wm[w * G + h];
-                if (mw != NEG) o += wO[w * G * D + e] * exp2f(mw - mh);
-            }
-        }
-        pub_o[e] = o;
-    }
-    if (tid < G) {
-        float mh = NEG, l = 0.f;
-        if (cnt > 0) {
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) mh = fmaxf(mh, wm[w * G + tid]);
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float mw = wm[w * G + tid];
-                if (mw != NEG) l += wl[w * G + tid] * exp2f(mw - mh);
-            }
-        } else {
-            mh = NEG;
-        }
-        pub_ml[tid] = make_float2(mh, l);
-    }
-    cluster_sync();  // #1: every chunk's state is published
-
-    for (int e = tid; e < nchunk * G; e += kConsumers) {
-        const uint32_t a = dsmem_addr(&pub_ml[e % G], static_cast<uint32_t>(e / G));
-        s_mlc[e] = make_float2(ld_dsmem_f32(a), ld_dsmem_f32(a + 4));
-    }
-    consumer_bar_sync();
-    // Thread e = (chunk c, head h) computes its own term of l_h =
-    // sum_c l_ch 2^(m_ch - m_h) (one exponential per thread, all at once),
-    // then reads the sum back; the same terms in the same order as a
-    // sequential loop over the chunks.
-    const bool ml_thread = tid < nchunk * G;  // nchunk * G <= kConsumers
-    const int h_e = tid % G;
-    float m_e = NEG, u_e = 0.f;
-    float2 v_e = make_float2(NEG, 0.f);
-    if (ml_thread) {
-        for (int c = 0; c < nchunk; ++c) m_e = fmaxf(m_e, s_mlc[c * G + h_e].x);
-        v_e = s_mlc[tid];
-        u_e = (v_e.x == NEG) ? 0.f : exp2f(v_e.x - m_e);
-        s_term[tid] = (v_e.x == NEG) ? 0.f : v_e.y * u_e;
-    }
-    consumer_bar_sync();
-    if (ml_thread) {
-        float l = 0.f;
-        for (int c = 0; c < nchunk; ++c) l += s_term[c * G + h_e];
-        const float il = (l > 0.f) ? 1.f / l : 0.f;
-        s_w[tid] = (v_e.x == NEG) ? 0.f : u_e * il;
-        if (tid < G) {
-            s_m[tid] = m_e;
-            s_il[tid] = il;
-        }
-    }
-    consumer_bar_sync();
-
-    // This CTA's slice of the output row: O_h = sum_c w_ch * O_ch.
-    {
-        const int b = u / p.Hkv;
-        const int kvh = u - b * p.Hkv;
-        __nv_bfloat16* out = p.out + (static_cast<size_t>(b) * p.Hq + kvh * G) * D;
-        const int per = (G * D + nchunk - 1) / nchunk;
-        const int e0 = static_cast<int>(rank) * per;
-        const int e1 = min(G * D, e0 + per);
-        for (int e = e0 + tid; e < e1; e += kConsumers) {
-            const int h = e / D;
-            // Every peer's value is requested before the first is used, so
-            // the remote loads share one round trip.
-            float v[kMaxClusterChunks];
-#pragma unroll
-            for (int c = 0; c < kMaxClusterChunks; ++c)
-                v[c] = (c < nchunk)
-                           ? ld_dsmem_f32(dsmem_addr(&pub_o[e], static_cast<uint32_t>(c)))
-                           : 0.f;
-            float o = 0.f;
-#pragma unroll
-            for (int c = 0; c < kMaxClusterChunks; ++c) {
-                if (c < nchunk) {
-                    const float w = s_w[c * G + h];
-                    o += (w != 0.f) ? w * v[c] : 0.f;
-                }
-            }
-            out[e] = __float2bfloat16_rn(o);
-        }
-    }
-
-    if constexpr (kScore) {
-        // LongFlowScore of this chunk's slots and their local best candidate.
-        float cexp[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) cexp[h] = __log2f(s_il[h]) - s_m[h];
-        uint32_t bkey;
-        int bestj;
-        score_chunk<G, kPreload>(p, u, slot0, n, ages, cexp, t0, tid, bkey, bestj);
-        warp_best(bkey, bestj);
-        const float* stash = p.stash + static_cast<size_t>(u) * p.S * G;
-        uint32_t* red_k = reinterpret_cast<uint32_t*>(red_v);
-        if ((tid & 31) == 0) {
-            red_k[tid >> 5] = bkey;
-            red_j[tid >> 5] = bestj;
-        }
-        consumer_bar_sync();
-        if (tid == 0) {
-            for (int w = 1; w < kConsumerWarps; ++w)
-                if (key_less(red_k[w], red_j[w], bkey, bestj)) {
-                    bkey = red_k[w];
-                    bestj = red_j[w];
-                }
-            st_dsmem_s32(dsmem_addr(&pub_best[rank], 0u), static_cast<int32_t>(bkey));
-            st_dsmem_s32(dsmem_addr(&pub_bestj[rank], 0u), bestj);
-        }
-        // This chunk's score terms are read: drop them from L2, no write-back.
-        discard_range(stash + static_cast<size_t>(slot0) * G, static_cast<size_t>(n) * G * 4, tid,
-                      kConsumers);
-    }
-    // #2: every peer's reads of this CTA's shared memory are done and every
-    // local best sits in rank 0's arrays; after it no CTA touches another's
-    // shared memory, so each may leave.
-    cluster_sync();
-
-    if (kScore && rank == 0 && tid == 0) {
-        uint32_t bkey = 0xffffffffu;
-        int bestj = 0x7fffffff;
-        for (int c = 0; c < nchunk; ++c) {
-            if (key_less(pub_best[c], pub_bestj[c], bkey, bestj)) {
-                bkey = pub_best[c];
-                bestj = pub_bestj[c];
-            }
-        }
-        const int slot = (bestj == 0x7fffffff) ? -1 : bestj;
-        p.next_slot[u] = slot;
-        if (slot >= 0 && (p.flags & kFlagMaskEvicted))
-            p.mask[static_cast<size_t>(u) * p.S + slot] = -1;
-    }
-}
-
 // Merge of a cluster unit by pushes (StepAlloc::kPush). The CTA merges its
-// four warps' online-softmax states in shared memory, then each consumer
-// thread stores one 16-byte piece of the merged output row into the CTA that
-// owns it (PushSmem) and the CTA's (m, l) per head into every CTA, with
-// asynchronous remote stores counted on the receiver's data barrier; each
-// warp arrives on its own CTA's barrier for the stores it made locally. Once
-// a CTA's barrier completes it holds every chunk's (m, l) and every chunk's
-// partial of the elements it owns: it writes those, scores its own chunk
-// with c_h = log2(1/l_h) - m_h, and sends its best (key, slot) to rank 0,
-// which reduces the cluster's argmin. No cluster barrier follows the main
-// loop: every store into a CTA is counted on one of its barriers, and a CTA
-// leaves only after its own have completed.
+// four warps' online-softmax states in shared memory, then sends the CTA's
+// (m, l) per head into every CTA and, one 16-byte piece per consumer thread,
+// its merged output row into the CTAs that own the pieces (PushSmem), with
+// asynchronous remote stores counted on the receiver's (m, l) and output
+// barriers; each warp arrives on its own CTA's barriers for the stores it
+// made locally. With every chunk's (m, l) a CTA scores its own chunk with
+// c_h = log2(1/l_h) - m_h and sends its best (key, slot) to rank 0 while the
+// output pieces land; then it writes the output elements it owns, and rank 0
+// reduces the cluster's argmin. No cluster barrier follows the main loop:
+// every store into a CTA is counted on one of its barriers, and a CTA leaves
+// only after its own have completed.
 template <int D, int G, int kStages, bool kScore>
 __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, int slot0, int n,
-                                                   const int32_t* ages, uint8_t* smem,
+                                                   const uint8_t* sflags, uint8_t* smem,
                                                    uint8_t* pbase, const float (&acc)[D / 16][4],
                                                    float m0, float m1, float l0, float l1,
                                                    int tid) {
@@ -1158,8 +990,9 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
     float* s_il = reinterpret_cast<float*>(pbase + P::kIlOff);
     uint32_t* red_k = reinterpret_cast<uint32_t*>(pbase + P::kRedOff);
     int* red_j = reinterpret_cast<int*>(red_k + kConsumerWarps);
-    uint64_t* bar_data = reinterpret_cast<uint64_t*>(pbase + P::kBarOff);
-    uint64_t* bar_best = bar_data + 1;
+    uint64_t* bar_ml = reinterpret_cast<uint64_t*>(pbase + P::kBarOff);
+    uint64_t* bar_o = bar_ml + 1;
+    uint64_t* bar_best = bar_ml + 2;
     float* wO = reinterpret_cast<float*>(smem);            // [4][G][kStride]
     float* wm = wO + kConsumerWarps * G * kStride;          // [4][G]
     float* wl = wm + kConsumerWarps * G;                    // [4][G]
@@ -1172,7 +1005,7 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
     // (held across it only where registers allow, as in cluster_epilogue).
     constexpr bool kPreload = kScore && (G <= 4 || kStages == kDeepStages);
     float t0[kScoreBatch][G];
-    if constexpr (kPreload) preload_terms<G>(p, u, slot0, n, ages, tid, t0);
+    if constexpr (kPreload) preload_terms<G>(p, u, slot0, n, sflags, tid, t0);
 
     // The four warps' states: lane (r, pair) holds heads h0 = 2 pair, h0 + 1
     // of rows mt * 16 + r and + 8 of every 16-row block.
@@ -1202,8 +1035,26 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
     // barrier begun at kernel start).
     cluster_wait();
 
-    // The CTA's merged output row, 4 elements per thread, each piece to the
-    // CTA that owns it; then (m, l) of head h to CTA c (thread c * G + h).
+    // The CTA's (m, l) of head h to CTA c (thread c * G + h), then its merged
+    // output row, 4 elements per thread, each piece to the CTA that owns it.
+    if (tid < nchunk * G) {
+        const int c = tid / G;
+        const int h = tid - c * G;
+        float mh = NEG, l = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) mh = fmaxf(mh, wm[w * G + h]);
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float mw = wm[w * G + h];
+            if (mw != NEG) l += wl[w * G + h] * exp2f(mw - mh);
+        }
+        float2* dst = &recv_ml[rank * G + h];
+        if (c == rank)
+            *dst = make_float2(mh, l);
+        else
+            st_async_v2(dsmem_addr(dst, c), __float_as_uint(mh), __float_as_uint(l),
+                        dsmem_addr(bar_ml, c));
+    }
     for (int e = 4 * tid; e < kElems; e += 4 * kConsumers) {
         const int h = e / D;
         const int d = e - h * D;
@@ -1231,33 +1082,18 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
         if (c == rank)
             *reinterpret_cast<float4*>(dst) = o;
         else
-            st_async_v4(dsmem_addr(dst, c), o.x, o.y, o.z, o.w, dsmem_addr(bar_data, c));
-    }
-    if (tid < nchunk * G) {
-        const int c = tid / G;
-        const int h = tid - c * G;
-        float mh = NEG, l = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) mh = fmaxf(mh, wm[w * G + h]);
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            const float mw = wm[w * G + h];
-            if (mw != NEG) l += wl[w * G + h] * exp2f(mw - mh);
-        }
-        float2* dst = &recv_ml[rank * G + h];
-        if (c == rank)
-            *dst = make_float2(mh, l);
-        else
-            st_async_v2(dsmem_addr(dst, c), __float_as_uint(mh), __float_as_uint(l),
-                        dsmem_addr(bar_data, c));
+            st_async_v4(dsmem_addr(dst, c), o.x, o.y, o.z, o.w, dsmem_addr(bar_o, c));
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar_data);  // this warp's local stores
-    // The barrier completes only when every store into this CTA has landed,
-    // so it takes the full limit even under a shortened diagnostic one: the
-    // CTA must not leave while a peer's stores are in flight. (A main loop
-    // that gave up still stores its partial state, so the wait ends.)
-    if (!mbar_wait_cluster(bar_data, 0) && lane == 0) atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
+    if (lane == 0) {  // this warp's local stores
+        mbar_arrive(bar_ml);
+        mbar_arrive(bar_o);
+    }
+    // These barriers complete only when every store into this CTA has
+    // landed, so they take the full limit even under a shortened diagnostic
+    // one: the CTA must not leave while a peer's stores are in flight. (A
+    // main loop that gave up still stores its partial state, so they end.)
+    if (!mbar_wait_cluster(bar_ml, 0) && lane == 0) atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
 
     // Per head (warp h): m_h over the chunks, l_h and every chunk's weight
     // 2^(m_c - m_h) / l_h.
@@ -1279,7 +1115,34 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
     }
     consumer_bar_sync();
 
+    // The chunk's scores and its best candidate, sent to rank 0.
+    uint32_t bkey = 0xffffffffu;
+    int bestj = 0x7fffffff;
+    if constexpr (kScore) {
+        float cexp[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) cexp[h] = __log2f(s_il[h]) - s_m[h];
+        score_chunk<G, kPreload>(p, u, slot0, n, sflags, cexp, t0, tid, bkey, bestj);
+        warp_best(bkey, bestj);
+        if (lane == 0) {
+            red_k[warp] = bkey;
+            red_j[warp] = bestj;
+        }
+        consumer_bar_sync();
+        if (tid == 0) {
+            for (int w = 1; w < kConsumerWarps; ++w)
+                if (key_less(red_k[w], red_j[w], bkey, bestj)) {
+                    bkey = red_k[w];
+                    bestj = red_j[w];
+                }
+            if (rank != 0)
+                st_async_v2(dsmem_addr(&recv_best[rank], 0u), bkey, static_cast<uint32_t>(bestj),
+                            dsmem_addr(bar_best, 0u));
+        }
+    }
+
     // The output elements this CTA owns: O_h = sum_c w_ch O_ch.
+    if (!mbar_wait_cluster(bar_o, 0) && lane == 0) atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
     {
         const int b = u / p.Hkv;
         const int kvh = u - b * p.Hkv;
@@ -1298,42 +1161,20 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
     }
 
     if constexpr (kScore) {
-        float cexp[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) cexp[h] = __log2f(s_il[h]) - s_m[h];
-        uint32_t bkey;
-        int bestj;
-        score_chunk<G, kPreload>(p, u, slot0, n, ages, cexp, t0, tid, bkey, bestj);
-        warp_best(bkey, bestj);
-        if (lane == 0) {
-            red_k[warp] = bkey;
-            red_j[warp] = bestj;
-        }
-        consumer_bar_sync();
-        if (tid == 0) {
-            for (int w = 1; w < kConsumerWarps; ++w)
-                if (key_less(red_k[w], red_j[w], bkey, bestj)) {
-                    bkey = red_k[w];
-                    bestj = red_j[w];
+        if (tid == 0 && rank == 0) {
+            if (nchunk > 1 && !mbar_wait_cluster(bar_best, 0))  // full limit, as above
+                atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
+            for (int c = 1; c < nchunk; ++c) {
+                const uint2 v = recv_best[c];
+                if (key_less(v.x, static_cast<int>(v.y), bkey, bestj)) {
+                    bkey = v.x;
+                    bestj = static_cast<int>(v.y);
                 }
-            if (rank != 0) {
-                st_async_v2(dsmem_addr(&recv_best[rank], 0u), bkey, static_cast<uint32_t>(bestj),
-                            dsmem_addr(bar_best, 0u));
-            } else {
-                if (nchunk > 1 && !mbar_wait_cluster(bar_best, 0))  // full limit, as above
-                    atomicOr(p.dev_err, LF_DEVERR_WAIT_TIMEOUT);
-                for (int c = 1; c < nchunk; ++c) {
-                    const uint2 v = recv_best[c];
-                    if (key_less(v.x, static_cast<int>(v.y), bkey, bestj)) {
-                        bkey = v.x;
-                        bestj = static_cast<int>(v.y);
-                    }
-                }
-                const int slot = (bestj == 0x7fffffff) ? -1 : bestj;
-                p.next_slot[u] = slot;
-                if (slot >= 0 && (p.flags & kFlagMaskEvicted))
-                    p.mask[static_cast<size_t>(u) * p.S + slot] = -1;
             }
+            const int slot = (bestj == 0x7fffffff) ? -1 : bestj;
+            p.next_slot[u] = slot;
+            if (slot >= 0 && (p.flags & kFlagMaskEvicted))
+                p.mask[static_cast<size_t>(u) * p.S + slot] = -1;
         }
         // This chunk's score terms are read: drop them from L2, no write-back.
         const float* stash = p.stash + (static_cast<size_t>(u) * p.S + slot0) * G;
@@ -1341,28 +1182,36 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
     }
 }
 
-// Expected bytes of a push-merge CTA's barriers, armed at kernel start: the
-// data barrier counts the remote stores of the other nchunk - 1 CTAs (the
-// elements this CTA owns and (m, l) per head from each); rank 0's best
-// barrier their (key, slot) pairs.
+// Arms a receive barrier for `bytes` bytes of remote stores (a plain arrival
+// when there are none).
+__device__ __forceinline__ void arm_receive(uint64_t* bar, uint32_t bytes) {
+    if (bytes > 0)
+        mbar_arrive_expect_tx(bar, bytes);
+    else
+        mbar_arrive(bar);
+}
+
+// The push merge's barriers, armed at kernel start with the bytes the other
+// nchunk - 1 CTAs store: their (m, l) per head, the output elements this CTA
+// owns and, at rank 0, their (key, slot) pairs. The (m, l) and output
+// barriers also count the four consumer warps' arrivals for their local
+// stores.
 template <int D, int G, bool kScore>
 __device__ __forceinline__ void push_barriers_init(uint8_t* pbase, int nchunk) {
     using P = PushSmem<D, G>;
-    uint64_t* bar_data = reinterpret_cast<uint64_t*>(pbase + P::kBarOff);
-    uint64_t* bar_best = bar_data + 1;
+    uint64_t* bar_ml = reinterpret_cast<uint64_t*>(pbase + P::kBarOff);
+    uint64_t* bar_o = bar_ml + 1;
+    uint64_t* bar_best = bar_ml + 2;
     const int rank = static_cast<int>(cluster_ctarank());
-    mbar_init(bar_data, 1 + kConsumerWarps);
+    mbar_init(bar_ml, 1 + kConsumerWarps);
+    mbar_init(bar_o, 1 + kConsumerWarps);
     mbar_init(bar_best, 1);
     const int per = P::per(nchunk);
-    const int own = max(0, min(per, P::kElems - rank * per));
-    const uint32_t per_src = static_cast<uint32_t>(own) * 4u + G * 8u;
-    if (nchunk > 1) {
-        mbar_arrive_expect_tx(bar_data, static_cast<uint32_t>(nchunk - 1) * per_src);
-        if (kScore && rank == 0)
-            mbar_arrive_expect_tx(bar_best, static_cast<uint32_t>(nchunk - 1) * 8u);
-    } else {
-        mbar_arrive(bar_data);
-    }
+    const uint32_t own = static_cast<uint32_t>(max(0, min(per, P::kElems - rank * per)));
+    const uint32_t peers = static_cast<uint32_t>(nchunk - 1);
+    arm_receive(bar_ml, peers * G * 8u);
+    arm_receive(bar_o, peers * own * 4u);
+    if (kScore && rank == 0) arm_receive(bar_best, peers * 8u);
 }
 
 // kStages-deep TMA ring; 3 stages run 2 CTAs per SM, 2 stages run 3.
@@ -1372,12 +1221,13 @@ template <int D, int G, int kStages, bool kScore, bool kCluster>
 __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2 : 1))
     lf_decode_step_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const StepParams p) {
-    using L = StepSmem<D, kStages>;
+    using L = StepSmem<D, kStages, kCluster>;
     using A = StepAlloc<D, G, kStages, kCluster>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    int32_t* ages = reinterpret_cast<int32_t*>(smem + L::kAgesOff);
+    using Slot = SlotState<kCluster>;
+    Slot* sflags = reinterpret_cast<Slot*>(smem + L::kFlagsOff);  // [n]
     // [0] bit mask of the chunk's tiles that hold a live slot, [1] abort flag,
     // [2] last-CTA flag
     volatile int32_t* misc = reinterpret_cast<int32_t*>(smem + L::kMiscOff);
@@ -1402,7 +1252,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         }
         misc[0] = 0;
         misc[1] = 0;
-        if constexpr (A::kPush) push_barriers_init<D, G, kScore>(smem + A::kPushOff, p.nchunk);
+        if constexpr (kCluster) push_barriers_init<D, G, kScore>(smem + A::kPushOff, p.nchunk);
         fence_barrier_init();
     }
     // The barriers are initialised before any thread may use them (the
@@ -1410,7 +1260,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     __syncthreads();
     // Push merge: peers may store into this CTA once every CTA of the
     // cluster has passed this point (waited for after the main loop).
-    if constexpr (A::kPush) cluster_arrive_relaxed();
+    if constexpr (kCluster) cluster_arrive_relaxed();
     // With programmatic dependent launch this CTA may start while the previous
     // kernel of the stream (often the previous decode step) is still running:
     // everything above touches only this CTA's shared memory; every global
@@ -1479,7 +1329,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     // Only the consumer threads age: their fence before the unit's arrival
     // counter (below) then also publishes the aged mask to the unit's last
     // CTA, and no fence delays the start of the pipeline. (Cluster CTAs read
-    // ages from shared memory only.)
+    // the slot flags from shared memory only.)
     constexpr int kPer = (kMaxChunkTiles * kTile + kConsumers - 1) / kConsumers;
     int32_t* mrow = p.mask + static_cast<size_t>(u) * S + slot0;
     const uint64_t mask_pol = l2_policy_evict_last();
@@ -1509,7 +1359,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
                 if (na != a) st_global_hint(mrow + i, na, mask_pol);
                 a = na;
             }
-            ages[i] = a;
+            sflags[i] = slot_state(a, p.W, sflags);
             if (a >= 0) live_bits |= 1u << (i / kTile);
         }
     }
@@ -1566,13 +1416,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
             for (int i = max(0, issued - kStages); i < issued; ++i)
                 (void)mbar_wait(&full[i % kStages], (i / kStages) & 1);
         }
-        if constexpr (A::kPush) {
-            cluster_wait();
-        } else if constexpr (kCluster) {
-            __syncwarp();
-            cluster_sync();  // the consumers' cluster barriers #1 and #2
-            cluster_sync();
-        }
+        if constexpr (kCluster) cluster_wait();  // the split barrier begun at kernel start
         return;
     }
 
@@ -1625,8 +1469,8 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
 
         const int iA = tslot0 - slot0 + wrow0 + r;
         const int iB = iA + 8;
-        const bool liveA = iA < n && ages[iA] >= 0;
-        const bool liveB = iB < n && ages[iB] >= 0;
+        const bool liveA = iA < n && slot_live(sflags[iA]);
+        const bool liveB = iB < n && slot_live(sflags[iB]);
 
         // Logits S^T and row norms ||v||_1 for this warp's 16 slots.
         // Grids of many waves split each product into two accumulator chains
@@ -1755,9 +1599,10 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-    if constexpr (A::kPush) {
-        static_assert(PushSmem<D, G>::kStageBytes <= L::kAgesOff, "warp states exceed the TMA ring");
-        cluster_merge_push<D, G, kStages, kScore>(p, u, slot0, n, ages, smem, smem + A::kPushOff,
+    if constexpr (kCluster) {
+        static_assert(A::kPush, "a cluster instance without room for the push merge");
+        static_assert(PushSmem<D, G>::kStageBytes <= L::kFlagsOff, "warp states exceed the TMA ring");
+        cluster_merge_push<D, G, kStages, kScore>(p, u, slot0, n, sflags, smem, smem + A::kPushOff,
                                                   acc, m0, m1, l0, l1, tid);
         return;
     }
@@ -1782,11 +1627,6 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         }
     }
     consumer_bar_sync();
-
-    if constexpr (kCluster) {
-        cluster_epilogue<D, G, kStages, kScore>(p, u, slot0, n, ages, smem, wO, wm, wl, cnt, tid);
-        return;
-    }
 
     const size_t pidx = static_cast<size_t>(u) * p.nchunk + chunk;
     if (cnt > 0) {

@@ -57,12 +57,14 @@
  *   LF_CHUNK_TILES=n   64-slot tiles per chunk of the slot axis (1..32);
  *                      a cluster merge may still re-chunk to its size cap
  *   LF_STAGES=3        three-stage TMA ring (two CTAs per SM) instead of two
- *   LF_CLUSTER=0|1     thread-block-cluster merge off / on wherever it fits
- *   LF_CLUSTER_MAX=n   largest cluster, 2..16 CTAs (default 16, a
- *                      non-portable size; 8 where 16 cannot be placed)
- *   LF_DEEP=0|1        cluster grids of at most one CTA per SM keep the
- *                      2-stage TMA ring / take the deep one even for chunks
- *                      of fewer than 5 tiles
+ *   LF_CLUSTER=0|1     thread-block-cluster merge off / on wherever one
+ *                      cluster of the split can be placed
+ *   LF_CLUSTER_MAX=n   largest cluster tried, 2..16 CTAs (default 16, a
+ *                      non-portable size; smaller ones where it cannot be
+ *                      placed)
+ *   LF_DEEP=0|1        cluster grids keep the 2-stage TMA ring / take the
+ *                      deep one (one CTA per SM) whenever its clusters all
+ *                      fit (default: the shorter modelled step)
  *   LF_PDL=0           programmatic dependent launch off
  *   LF_SPEC=0          the grid's first wave waits for the live-tile list
  *                      before loading tiles (no speculative first tiles)

@@ -142,8 +142,9 @@ struct PushSmem {
     static constexpr int kRedOff = kIlOff + G * 4;                      // 2 x [4 warps]
     static constexpr int kBarOff = (kRedOff + 2 * kConsumerWarps * 4 + 7) & ~7;
     static constexpr int kBytes = kBarOff + 24;  // (m, l), output and best barriers
-    // The four warps' states, staged in the drained TMA ring: output rows
-    // with a padded stride (conflict-free stores), then (m, l).
+    // The four warps' states, staged in the drained TMA ring (the deep ring:
+    // beside the receive buffers): output rows with a padded stride
+    // (conflict-free stores), then (m, l).
     static constexpr int kStride = D + 4;
     static constexpr int kStageBytes = (kConsumerWarps * G * kStride + 2 * kConsumerWarps * G) * 4;
 };
@@ -155,7 +156,11 @@ struct StepAlloc {
     using L = StepSmem<D, kStages, kCluster>;
     using P = PushSmem<D, G>;
     static constexpr int kPushOff = (L::kBytes + 15) & ~15;
-    static constexpr int kPushAlloc = kPushOff + P::kBytes + 1024;
+    // The deep ring also stages the four warps' states beside the receive
+    // buffers, outside the ring (cluster_merge_push).
+    static constexpr int kStageOff = kPushOff + ((P::kBytes + 15) & ~15);
+    static constexpr int kPushAlloc =
+        kStageOff + (kStages == kDeepStages ? P::kStageBytes : 0) + 1024;
     static constexpr int kPerSm = kStages == 2 ? 3 : (kStages == 3 ? 2 : 1);
     // 227 KB per CTA at most; 228 KB per SM, 1 KB of it reserved per CTA.
     static constexpr bool kPush =
@@ -943,17 +948,14 @@ __device__ __forceinline__ void score_chunk(const StepParams& p, int u, int slot
     }
 }
 
-// The warp's lexicographic (key, slot) minimum, in every lane.
-__device__ __forceinline__ void warp_best(uint32_t& bkey, int& bestj) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const uint32_t ok = __shfl_xor_sync(0xffffffffu, bkey, off);
-        const int oj = __shfl_xor_sync(0xffffffffu, bestj, off);
-        if (key_less(ok, oj, bkey, bestj)) {
-            bkey = ok;
-            bestj = oj;
-        }
-    }
+// The warp's lexicographic (key, slot) minimum, in every lane, by two warp
+// reductions: the least key, then the least slot among the lanes holding it.
+__device__ __forceinline__ void warp_best_redux(uint32_t& bkey, int& bestj) {
+    const uint32_t kmin = __reduce_min_sync(0xffffffffu, bkey);
+    const uint32_t jmin = __reduce_min_sync(
+        0xffffffffu, bkey == kmin ? static_cast<uint32_t>(bestj) : 0xffffffffu);
+    bkey = kmin;
+    bestj = static_cast<int>(jmin);
 }
 
 // Merge of a cluster unit by pushes (StepAlloc::kPush). The CTA merges its
@@ -971,7 +973,8 @@ __device__ __forceinline__ void warp_best(uint32_t& bkey, int& bestj) {
 template <int D, int G, int kStages, bool kScore>
 __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, int slot0, int n,
                                                    const uint8_t* sflags, uint8_t* smem,
-                                                   uint8_t* pbase, const float (&acc)[D / 16][4],
+                                                   uint8_t* pbase, uint8_t* wstage,
+                                                   const float (&acc)[D / 16][4],
                                                    float m0, float m1, float l0, float l1,
                                                    int tid) {
     using P = PushSmem<D, G>;
@@ -993,19 +996,25 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
     uint64_t* bar_ml = reinterpret_cast<uint64_t*>(pbase + P::kBarOff);
     uint64_t* bar_o = bar_ml + 1;
     uint64_t* bar_best = bar_ml + 2;
-    float* wO = reinterpret_cast<float*>(smem);            // [4][G][kStride]
-    float* wm = wO + kConsumerWarps * G * kStride;          // [4][G]
-    float* wl = wm + kConsumerWarps * G;                    // [4][G]
+    // The deep ring stages the warps' states outside the ring, so they need
+    // no barrier before it; the others wait until every warp is done with
+    // the ring.
+    constexpr bool kStageOutside = kStages == kDeepStages;
+    float* wO = reinterpret_cast<float*>(kStageOutside ? wstage : smem);  // [4][G][kStride]
+    float* wm = wO + kConsumerWarps * G * kStride;                        // [4][G]
+    float* wl = wm + kConsumerWarps * G;                                  // [4][G]
     const float NEG = -INFINITY;
 
-    // Every warp is done with the ring, and every slot's score terms (stored
-    // by the warp that owns its row) are ordered before the loads below.
-    consumer_bar_sync();
     // The chunk's first batch of score terms, requested before the merge
-    // (held across it only where registers allow, as in cluster_epilogue).
+    // (held across it only where registers allow). Every slot's terms were
+    // stored by the warp that owns its row: a barrier orders them before
+    // these loads.
     constexpr bool kPreload = kScore && (G <= 4 || kStages == kDeepStages);
     float t0[kScoreBatch][G];
-    if constexpr (kPreload) preload_terms<G>(p, u, slot0, n, sflags, tid, t0);
+    if constexpr (!kStageOutside) {
+        consumer_bar_sync();
+        if constexpr (kPreload) preload_terms<G>(p, u, slot0, n, sflags, tid, t0);
+    }
 
     // The four warps' states: lane (r, pair) holds heads h0 = 2 pair, h0 + 1
     // of rows mt * 16 + r and + 8 of every 16-row block.
@@ -1030,6 +1039,7 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
         }
     }
     consumer_bar_sync();
+    if constexpr (kStageOutside && kPreload) preload_terms<G>(p, u, slot0, n, sflags, tid, t0);
 
     // Every CTA of the cluster has initialised its barriers (the split
     // barrier begun at kernel start).
@@ -1123,7 +1133,7 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
 #pragma unroll
         for (int h = 0; h < G; ++h) cexp[h] = __log2f(s_il[h]) - s_m[h];
         score_chunk<G, kPreload>(p, u, slot0, n, sflags, cexp, t0, tid, bkey, bestj);
-        warp_best(bkey, bestj);
+        warp_best_redux(bkey, bestj);
         if (lane == 0) {
             red_k[warp] = bkey;
             red_j[warp] = bestj;
@@ -1603,7 +1613,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         static_assert(A::kPush, "a cluster instance without room for the push merge");
         static_assert(PushSmem<D, G>::kStageBytes <= L::kFlagsOff, "warp states exceed the TMA ring");
         cluster_merge_push<D, G, kStages, kScore>(p, u, slot0, n, sflags, smem, smem + A::kPushOff,
-                                                  acc, m0, m1, l0, l1, tid);
+                                                  smem + A::kStageOff, acc, m0, m1, l0, l1, tid);
         return;
     }
     consumer_bar_sync();  // every consumer is done with the stage buffers

@@ -352,7 +352,10 @@ Plan plan_split(int S, int units, int sms, bool want_cluster, int D, int G, bool
                 const int f2 = lf::max_active_clusters(D, G, 2, score, nc);
                 if (first.nc == 0) first = {ct, nc, f2};
                 if (two.nc == 0 && units <= f2) two = {ct, nc, f2};
-                if (dmode != 0 && deep.nc == 0) {
+                // (The deep ring keeps a chunk's score terms in shared memory,
+                // which bounds its chunk.)
+                if (dmode != 0 && deep.nc == 0 &&
+                    (!score || ct * lf::kTile <= lf::deep_term_slots(D, G))) {
                     const int fd = lf::max_active_clusters(D, G, lf::kDeepStages, score, nc);
                     if (units <= fd) deep = {ct, nc, fd};
                 }

@@ -57,6 +57,15 @@ int max_active_clusters(int D, int G, int stages, bool score, int csize) {
     return n;
 }
 
+int deep_term_slots(int D, int G) {
+#define LF_STEP_CASE(DD, GG) \
+    if (D == DD && G == GG) return StepAlloc<DD, GG, kDeepStages, true>::kTermSlots;
+    LF_STEP_CASE(64, 1) LF_STEP_CASE(64, 2) LF_STEP_CASE(64, 4) LF_STEP_CASE(64, 8)
+    LF_STEP_CASE(128, 1) LF_STEP_CASE(128, 2) LF_STEP_CASE(128, 4) LF_STEP_CASE(128, 8)
+#undef LF_STEP_CASE
+    return 0;
+}
+
 cudaError_t launch_decode_step_cluster(int D, int G, int stages, bool score,
                                        const CUtensorMap& tmK, const CUtensorMap& tmV,
                                        const StepParams& p, int units, cudaStream_t stream,

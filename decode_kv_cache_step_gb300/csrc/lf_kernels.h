@@ -98,6 +98,10 @@ cudaError_t launch_decode_step_cluster(int D, int G, int stages, bool score,
 // 0 if none can or the query fails. Cached per device and instance.
 int max_active_clusters(int D, int G, int stages, bool score, int csize);
 
+// Slots of a chunk whose score terms the deep-ring cluster instance keeps
+// in shared memory (the plan gives that ring no longer chunks).
+int deep_term_slots(int D, int G);
+
 // The scoring kernel of a split finish: grid (parts, units); CTA (c, u)
 // waits for unit u's ready flag, scores its chunks from the ages, the score
 // terms and c_h, and the unit's last CTA writes next_slot (and masks it with

@@ -159,13 +159,25 @@ struct StepAlloc {
     // The deep ring also stages the four warps' states beside the receive
     // buffers, outside the ring (cluster_merge_push).
     static constexpr int kStageOff = kPushOff + ((P::kBytes + 15) & ~15);
-    static constexpr int kPushAlloc =
-        kStageOff + (kStages == kDeepStages ? P::kStageBytes : 0) + 1024;
+    static constexpr int kTermOff =
+        kStageOff + ((kStages == kDeepStages ? P::kStageBytes : 0) + 15) / 16 * 16;
+    static constexpr int kPushAlloc = kTermOff + 1024;
     static constexpr int kPerSm = kStages == 2 ? 3 : (kStages == 3 ? 2 : 1);
     // 227 KB per CTA at most; 228 KB per SM, 1 KB of it reserved per CTA.
     static constexpr bool kPush =
         kCluster && kPushAlloc <= 232448 && kPerSm * (kPushAlloc + 1024) <= 233472;
-    static constexpr int kAlloc = kPush ? kPushAlloc : L::kAlloc;
+    // The deep ring (one CTA per SM) keeps the chunk's score terms in what is
+    // left of shared memory: [n][G] floats for chunks of up to kTermSlots
+    // slots (the plan gives it no longer chunks).
+    static constexpr bool kSmemTerms = kPush && kStages == kDeepStages;
+    static constexpr int term_bytes() {
+        const int m = (232448 - kPushAlloc) / 16 * 16;
+        const int most = kMaxChunkTiles * kTile * G * 4;
+        return m < 0 ? 0 : (m < most ? m : most);
+    }
+    static constexpr int kTermBytes = kSmemTerms ? term_bytes() : 0;
+    static constexpr int kTermSlots = kTermBytes / (G * 4);
+    static constexpr int kAlloc = kPush ? kPushAlloc + kTermBytes : L::kAlloc;
 };
 
 __device__ __forceinline__ void consumer_bar_sync() {
@@ -257,6 +269,27 @@ __device__ __forceinline__ void load_terms(const float* t, float (&v)[G]) {
 #pragma unroll
         for (int q = 0; q < G / 4; ++q) {
             const float4 a = __ldcg(reinterpret_cast<const float4*>(t) + q);
+            v[4 * q] = a.x;
+            v[4 * q + 1] = a.y;
+            v[4 * q + 2] = a.z;
+            v[4 * q + 3] = a.w;
+        }
+    }
+}
+
+// The same from the chunk's term array in shared memory.
+template <int G>
+__device__ __forceinline__ void load_terms_smem(const float* t, float (&v)[G]) {
+    if constexpr (G == 1) {
+        v[0] = t[0];
+    } else if constexpr (G == 2) {
+        const float2 a = *reinterpret_cast<const float2*>(t);
+        v[0] = a.x;
+        v[1] = a.y;
+    } else {
+#pragma unroll
+        for (int q = 0; q < G / 4; ++q) {
+            const float4 a = reinterpret_cast<const float4*>(t)[q];
             v[4 * q] = a.x;
             v[4 * q + 1] = a.y;
             v[4 * q + 2] = a.z;
@@ -900,11 +933,12 @@ __device__ __forceinline__ void preload_terms(const StepParams& p, int u, int sl
 // score export, and the thread's best candidate (key, slot): key 0xffffffff
 // and slot 0x7fffffff when it has none. t0 holds the first batch when
 // kPreloaded.
-template <int G, bool kPreloaded>
+template <int G, bool kPreloaded, bool kSmemTerms = false>
 __device__ __forceinline__ void score_chunk(const StepParams& p, int u, int slot0, int n,
                                             const uint8_t* sflags, const float (&cexp)[G],
                                             const float (&t0)[kScoreBatch][G], int tid,
-                                            uint32_t& bkey, int& bestj) {
+                                            uint32_t& bkey, int& bestj,
+                                            const float* sterm = nullptr) {
     const int S = p.S;
     const float* stash = p.stash + static_cast<size_t>(u) * S * G;
     float* scores = p.scores ? p.scores + static_cast<size_t>(u) * S : nullptr;
@@ -925,8 +959,12 @@ __device__ __forceinline__ void score_chunk(const StepParams& p, int u, int slot
 #pragma unroll
             for (int k = 0; k < kScoreBatch; ++k) {
                 const int i = i0 + k * kConsumers;
-                if (i < n && (sflags[i] & kSlotLive))
-                    load_terms<G>(stash + static_cast<size_t>(slot0 + i) * G, t[k]);
+                if (i < n && (sflags[i] & kSlotLive)) {
+                    if constexpr (kSmemTerms)
+                        load_terms_smem<G>(sterm + i * G, t[k]);
+                    else
+                        load_terms<G>(stash + static_cast<size_t>(slot0 + i) * G, t[k]);
+                }
             }
         }
 #pragma unroll
@@ -970,10 +1008,11 @@ __device__ __forceinline__ void warp_best_redux(uint32_t& bkey, int& bestj) {
 // reduces the cluster's argmin. No cluster barrier follows the main loop:
 // every store into a CTA is counted on one of its barriers, and a CTA leaves
 // only after its own have completed.
-template <int D, int G, int kStages, bool kScore>
+template <int D, int G, int kStages, bool kScore, bool kSmemTerms>
 __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, int slot0, int n,
                                                    const uint8_t* sflags, uint8_t* smem,
                                                    uint8_t* pbase, uint8_t* wstage,
+                                                   const float* sterm,
                                                    const float (&acc)[D / 16][4],
                                                    float m0, float m1, float l0, float l1,
                                                    int tid) {
@@ -1009,7 +1048,7 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
     // (held across it only where registers allow). Every slot's terms were
     // stored by the warp that owns its row: a barrier orders them before
     // these loads.
-    constexpr bool kPreload = kScore && (G <= 4 || kStages == kDeepStages);
+    constexpr bool kPreload = kScore && !kSmemTerms && (G <= 4 || kStages == kDeepStages);
     float t0[kScoreBatch][G];
     if constexpr (!kStageOutside) {
         consumer_bar_sync();
@@ -1132,7 +1171,9 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
         float cexp[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) cexp[h] = __log2f(s_il[h]) - s_m[h];
-        score_chunk<G, kPreload>(p, u, slot0, n, sflags, cexp, t0, tid, bkey, bestj);
+        // (Terms in shared memory: the barrier after the staging ordered them.)
+        score_chunk<G, kPreload, kSmemTerms>(p, u, slot0, n, sflags, cexp, t0, tid, bkey, bestj,
+                                             sterm);
         warp_best_redux(bkey, bestj);
         if (lane == 0) {
             red_k[warp] = bkey;
@@ -1187,8 +1228,10 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
                 p.mask[static_cast<size_t>(u) * p.S + slot] = -1;
         }
         // This chunk's score terms are read: drop them from L2, no write-back.
-        const float* stash = p.stash + (static_cast<size_t>(u) * p.S + slot0) * G;
-        discard_range(stash, static_cast<size_t>(n) * G * 4, tid, kConsumers);
+        if constexpr (!kSmemTerms) {
+            const float* stash = p.stash + (static_cast<size_t>(u) * p.S + slot0) * G;
+            discard_range(stash, static_cast<size_t>(n) * G * 4, tid, kConsumers);
+        }
     }
 }
 
@@ -1238,6 +1281,8 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     using Slot = SlotState<kCluster>;
     Slot* sflags = reinterpret_cast<Slot*>(smem + L::kFlagsOff);  // [n]
+    // The deep ring's score terms stay in shared memory ([n][G]).
+    float* sterm = reinterpret_cast<float*>(smem + A::kTermOff);
     // [0] bit mask of the chunk's tiles that hold a live slot, [1] abort flag,
     // [2] last-CTA flag
     volatile int32_t* misc = reinterpret_cast<int32_t*>(smem + L::kMiscOff);
@@ -1550,7 +1595,9 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
         // Per-slot score terms t = log2(exp(s) * ||v||_1).
         if (kScore && hv0) {
             const int slotA = tslot0 + wrow0 + r;
-            float* st = p.stash + (static_cast<size_t>(u) * S + slotA) * G + h0;
+            float* st = A::kSmemTerms
+                            ? sterm + (slotA - slot0) * G + h0
+                            : p.stash + (static_cast<size_t>(u) * S + slotA) * G + h0;
             if (liveA) {
                 const float lv = __log2f(nv[0]);
                 if (G == 1) st[0] = x0 + lv;
@@ -1631,8 +1678,9 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     if constexpr (kCluster) {
         static_assert(A::kPush, "a cluster instance without room for the push merge");
         static_assert(PushSmem<D, G>::kStageBytes <= L::kFlagsOff, "warp states exceed the TMA ring");
-        cluster_merge_push<D, G, kStages, kScore>(p, u, slot0, n, sflags, smem, smem + A::kPushOff,
-                                                  smem + A::kStageOff, acc, m0, m1, l0, l1, tid);
+        cluster_merge_push<D, G, kStages, kScore, A::kSmemTerms>(
+            p, u, slot0, n, sflags, smem, smem + A::kPushOff, smem + A::kStageOff, sterm, acc, m0,
+            m1, l0, l1, tid);
         return;
     }
     consumer_bar_sync();  // every consumer is done with the stage buffers

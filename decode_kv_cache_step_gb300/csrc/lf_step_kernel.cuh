@@ -948,40 +948,75 @@ __device__ __forceinline__ void score_chunk(const StepParams& p, int u, int slot
     // fill-empty-first) keeps the lowest slot among equal keys.
     bkey = 0xffffffffu;
     bestj = 0x7fffffff;
-    for (int i0 = tid; i0 < n; i0 += kScoreBatch * kConsumers) {
-        float t[kScoreBatch][G];
-        if (kPreloaded && i0 == tid) {
+    if constexpr (kSmemTerms) {
+        // Terms in shared memory: two slots per thread and round, both
+        // computed without a branch between them, so their dependent chains
+        // interleave (one warp per SM sub-partition hides no latency here).
+        constexpr int kB = 2;
+        for (int i0 = tid; i0 < n; i0 += kB * kConsumers) {
+            float L[kB], t[kB][G];
+            int f[kB];
 #pragma unroll
-            for (int k = 0; k < kScoreBatch; ++k)
-#pragma unroll
-                for (int h = 0; h < G; ++h) t[k][h] = t0[k][h];
-        } else {
-#pragma unroll
-            for (int k = 0; k < kScoreBatch; ++k) {
+            for (int k = 0; k < kB; ++k) {
                 const int i = i0 + k * kConsumers;
-                if (i < n && (sflags[i] & kSlotLive)) {
-                    if constexpr (kSmemTerms)
-                        load_terms_smem<G>(sterm + i * G, t[k]);
-                    else
-                        load_terms<G>(stash + static_cast<size_t>(slot0 + i) * G, t[k]);
+                f[k] = (i < n) ? sflags[i] : 0;
+                if (f[k] & kSlotLive) {
+                    load_terms_smem<G>(sterm + i * G, t[k]);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) t[k][h] = -INFINITY;
+                }
+                L[k] = log2_score<G>(t[k], cexp);
+            }
+#pragma unroll
+            for (int k = 0; k < kB; ++k) {
+                const int i = i0 + k * kConsumers;
+                if (i < n) {
+                    const int j = slot0 + i;
+                    const bool live = (f[k] & kSlotLive) != 0;
+                    const bool cand = live ? ((f[k] & kSlotOld) && L[k] == L[k]) : fill_first;
+                    const uint32_t key = live ? ordered_key(L[k]) : 0u;
+                    if (cand && key < bkey) {
+                        bkey = key;
+                        bestj = j;
+                    }
+                    if (scores)
+                        scores[j] = live ? exported_score<G>(p, L[k], t[k], cexp) : INFINITY;
                 }
             }
         }
+    } else {
+        for (int i0 = tid; i0 < n; i0 += kScoreBatch * kConsumers) {
+            float t[kScoreBatch][G];
+            if (kPreloaded && i0 == tid) {
 #pragma unroll
-        for (int k = 0; k < kScoreBatch; ++k) {
-            const int i = i0 + k * kConsumers;
-            if (i >= n) break;
-            const int f = sflags[i];
-            const int j = slot0 + i;
-            const float L = log2_score<G>(t[k], cexp);
-            const bool live = (f & kSlotLive) != 0;
-            const bool cand = live ? ((f & kSlotOld) && L == L) : fill_first;
-            const uint32_t key = live ? ordered_key(L) : 0u;
-            if (cand && key < bkey) {
-                bkey = key;
-                bestj = j;
+                for (int k = 0; k < kScoreBatch; ++k)
+#pragma unroll
+                    for (int h = 0; h < G; ++h) t[k][h] = t0[k][h];
+            } else {
+#pragma unroll
+                for (int k = 0; k < kScoreBatch; ++k) {
+                    const int i = i0 + k * kConsumers;
+                    if (i < n && (sflags[i] & kSlotLive))
+                        load_terms<G>(stash + static_cast<size_t>(slot0 + i) * G, t[k]);
+                }
             }
-            if (scores) scores[j] = live ? exported_score<G>(p, L, t[k], cexp) : INFINITY;
+#pragma unroll
+            for (int k = 0; k < kScoreBatch; ++k) {
+                const int i = i0 + k * kConsumers;
+                if (i >= n) break;
+                const int f = sflags[i];
+                const int j = slot0 + i;
+                const float L = log2_score<G>(t[k], cexp);
+                const bool live = (f & kSlotLive) != 0;
+                const bool cand = live ? ((f & kSlotOld) && L == L) : fill_first;
+                const uint32_t key = live ? ordered_key(L) : 0u;
+                if (cand && key < bkey) {
+                    bkey = key;
+                    bestj = j;
+                }
+                if (scores) scores[j] = live ? exported_score<G>(p, L, t[k], cexp) : INFINITY;
+            }
         }
     }
 }

@@ -1237,11 +1237,18 @@ __device__ __forceinline__ void cluster_merge_push(const StepParams& p, int u, i
         const int cnt = min(per, kElems - e0);
         for (int e = tid; e < cnt; e += kConsumers) {
             const int h = (e0 + e) / D;
-            float o = 0.f;
-            for (int c = 0; c < nchunk; ++c) {
-                const float wt = s_w[c * G + h];
-                o += (wt != 0.f) ? wt * recv_o[c * per + e] : 0.f;
+            // Every chunk's weight and partial are loaded before the first is
+            // used (a predicated unroll over the largest cluster), then summed
+            // in chunk order.
+            float wv[kMaxClusterChunks], ov[kMaxClusterChunks];
+#pragma unroll
+            for (int c = 0; c < kMaxClusterChunks; ++c) {
+                wv[c] = (c < nchunk) ? s_w[c * G + h] : 0.f;
+                ov[c] = (c < nchunk) ? recv_o[c * per + e] : 0.f;
             }
+            float o = 0.f;
+#pragma unroll
+            for (int c = 0; c < kMaxClusterChunks; ++c) o += (wv[c] != 0.f) ? wv[c] * ov[c] : 0.f;
             out[e0 + e] = __float2bfloat16_rn(o);
         }
     }

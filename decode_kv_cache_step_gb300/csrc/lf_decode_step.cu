@@ -150,12 +150,14 @@ __global__ void __launch_bounds__(kScoreThreads, G >= 8 ? 4 : 8) lf_score_kernel
         for (int w = 1; w < kScoreWarps; ++w) best = s_red[w] > best ? s_red[w] : best;
         bool last = true;
         if (parts > 1) {
-            if (best) atomicMax(&p.best[u], best);
-            __threadfence();
-            last = atomicAdd(&p.score_arrivals[u], 1u) == static_cast<uint32_t>(parts - 1);
+            // The maximum needs no returned value; the acquire-release add
+            // orders it before this CTA's arrival, and the unit's last CTA
+            // acquires every other CTA's maximum with its own add.
+            if (best) red_max_relaxed_gpu(&p.best[u], best);
+            last = atom_add_acq_rel_gpu(&p.score_arrivals[u], 1u) ==
+                   static_cast<uint32_t>(parts - 1);
             if (last) {
                 p.score_arrivals[u] = 0u;
-                __threadfence();
                 best = atomicExch(&p.best[u], 0ull);
             }
         }

@@ -34,6 +34,23 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* a, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
 }
 
+// Atomic add with acquire-release semantics at GPU scope; returns the old
+// value. After a CTA barrier, one thread's release covers the whole CTA's
+// earlier writes, and its acquire, followed by a barrier, the whole CTA's
+// later reads.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* a, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// 64-bit atomic maximum without a returned value (no round trip to wait
+// for); a later release by the same thread orders it.
+__device__ __forceinline__ void red_max_relaxed_gpu(unsigned long long* a, unsigned long long v) {
+    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -601,10 +601,7 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int usabl
             // counter, the chunks' score terms and ages).
             if (tid < G) p.cfold[static_cast<size_t>(u) * G + tid] = __log2f(s_il[tid]) - s_m[tid];
             consumer_bar_sync();
-            if (tid == 0) {
-                __threadfence();
-                st_release_gpu(p.ready + u, 1u);
-            }
+            if (tid == 0) st_release_gpu(p.ready + u, 1u);  // after the barrier: the CTA's writes
         } else {
             score_and_select<G>(p, u, s_m, s_il, red_v, red_j, s_ncand, s_live, topk_area,
                                 scan_area, scan_bytes, scan_bars, tid);
@@ -1780,12 +1777,16 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     }
 
     // ---------------------------------------- last CTA of the unit merges --
-    __threadfence();
+    // One acquire-release add on the unit's arrival counter after a CTA
+    // barrier releases every consumer's writes (partials, score terms, aged
+    // mask entries) to the unit's last CTA, whose same add acquires all the
+    // other chunks' (its barrier below passes that on to its threads); no
+    // thread waits for a fence of its own.
     consumer_bar_sync();
     if (tid == 0) {
         int last = 1;
         if (p.nchunk > 1) {
-            const uint32_t prev = atomicAdd(&p.arrivals[u], 1u);
+            const uint32_t prev = atom_add_acq_rel_gpu(&p.arrivals[u], 1u);
             last = (prev == static_cast<uint32_t>(p.nchunk - 1));
             if (last) p.arrivals[u] = 0u;  // every chunk of the unit has arrived
         }
@@ -1793,7 +1794,6 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     }
     consumer_bar_sync();
     if (!misc[2]) return;
-    __threadfence();
     finish_unit<D, G, kScore>(p, u, smem, L::kBarOff,
                               reinterpret_cast<uint64_t*>(smem + L::kScanBarOff), tid);
 }

@@ -306,7 +306,10 @@ Plan plan_split(int S, int units, int sms, bool want_cluster, int D, int G, bool
     // resident at once merges inside thread-block clusters: the
     // latency-bound small batches gain the shorter merge. Larger grids keep
     // the last-CTA merge, where a finished CTA frees its slot at once instead
-    // of waiting for its cluster. A cluster must sit within one GPC, so how
+    // of waiting for its cluster (measured with clusters forced on the full
+    // batches, same chunks, per step: the Fig. 1 shape 264.8 us against
+    // 240.4, the ragged 2400-slot batch 269.0 against 234.7, the 16K-slot
+    // workload 284.9 against 193.4). A cluster must sit within one GPC, so how
     // many fit at once comes from the occupancy query, not the SM count
     // (measured: 16 clusters of 8 one-per-SM CTAs, 128 of 152 SMs, took two
     // waves: 21.6 us per step against 10.4 for one cluster).

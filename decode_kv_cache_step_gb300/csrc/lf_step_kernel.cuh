@@ -1439,10 +1439,11 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     // is issued before any store, so the chunk's mask costs one round trip.
     // The aged entries are stored evict-last: the next step reads them again,
     // and between the two the K/V stream passes through L2 evict-first.
-    // Only the consumer threads age: their fence before the unit's arrival
-    // counter (below) then also publishes the aged mask to the unit's last
-    // CTA, and no fence delays the start of the pipeline. (Cluster CTAs read
-    // the slot flags from shared memory only.)
+    // Only the consumer threads age: the consumer barrier and the
+    // acquire-release add on the unit's arrival counter (below) then also
+    // publish the aged mask to the unit's last CTA, and nothing delays the
+    // start of the pipeline. (Cluster CTAs read the slot flags from shared
+    // memory only.)
     constexpr int kPer = (kMaxChunkTiles * kTile + kConsumers - 1) / kConsumers;
     int32_t* mrow = p.mask + static_cast<size_t>(u) * S + slot0;
     const uint64_t mask_pol = l2_policy_evict_last();

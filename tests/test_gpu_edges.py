@@ -1,8 +1,9 @@
 """GPU edge cases against the fp64 oracle: every supported head dim and
 group size, ragged slot counts that leave partial tiles, masked and empty
 units, writes into masked slots, garbage in masked slots, invalid write
-slots, protected windows, ties, the largest supported cache, argument
-errors, and concurrent streams."""
+slots, protected windows, ties, the largest supported cache (also at the
+widest group), the most units a launch takes, argument errors, and
+concurrent streams."""
 import numpy as np
 import pytest
 import torch
@@ -137,6 +138,26 @@ def test_largest_supported_cache():
             "mask": (S - 1 - np.arange(S, dtype=np.int32)).reshape(1, 1, S),
             "write_slot": np.array([[12345]], dtype=np.int32)}
     check_case(case, W=128, scale=0.125, where="S=2^20")
+
+
+def test_largest_cache_widest_group():
+    """S = 2^20 at d = 128 and g = 8: the split finish over 16384 tiles, with
+    the largest score-term scratch a unit takes."""
+    rng = np.random.default_rng(12)
+    S = 1 << 20
+    case = _pins.rand_case(rng, 1, 8, 1, 128, S, p_masked=0.3, max_age=3 * S, ws_mode="any")
+    p = lf.step_plan(1, 8, 1, 128, S)
+    assert p["split"] and not p["cluster"], p
+    check_case(case, W=128, scale=float(np.float32(1 / np.sqrt(128))), where="S=2^20 d=128 g=8")
+
+
+def test_most_units():
+    """B * Hkv = 65535, the most units one launch takes (the grid's y extent),
+    with a ragged last tile."""
+    rng = np.random.default_rng(13)
+    B, Hq, Hkv, d, S = 65535, 2, 1, 64, 70
+    case = _pins.rand_case(rng, B, Hq, Hkv, d, S, p_masked=0.2, max_age=200, ws_mode="any")
+    check_case(case, W=4, scale=0.125, where="65535 units")
 
 
 def test_argument_errors():

@@ -1705,6 +1705,11 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
                 mma_bf16_16816(acc[mt], a, pb0, pb1);
             }
         }
+        // The stage goes back to the producer as the iteration's last step,
+        // after every use of what was loaded from it. (A variant that released
+        // it earlier and stored the score terms after the release, with their
+        // norms loaded from this stage, gave outputs that differed from run to
+        // run in the last bits; a block fence before the release removed it.)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }

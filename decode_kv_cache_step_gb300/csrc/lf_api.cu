@@ -256,6 +256,7 @@ struct Plan {
     int tiles, chunk_tiles, nchunk, stages;
     bool cluster;  // the unit's chunks run as one thread-block cluster
     bool split;    // a top-1 step scores in a second kernel (split finish)
+    int split_from = 0;  // with split: units below this still scan in their last CTA
     int fit = 0;   // clusters that can be resident at once: of the plan's size with a
                    // cluster merge, else of the largest size tried (-1: not considered)
 };
@@ -391,6 +392,22 @@ Plan plan_split(int S, int units, int sms, bool want_cluster, int D, int G, bool
     const char* senv = std::getenv("LF_SPLIT");
     const int smode = senv ? std::atoi(senv) : -1;
     pl.split = want_cluster && !pl.cluster && smode != 0 && (smode == 1 || S >= kSplitMinSlots);
+    // A split grid of many waves merges its first units long before the
+    // scoring kernel can start (it starts with the decode grid's last wave),
+    // and by then their score terms have left L2. So the first 3/8 of the
+    // units still scan in their last CTA while their terms are in L2, and
+    // the scoring kernel takes the rest (measured on the 16K-slot workload,
+    // 256 units of 16 chunks, about 9 waves; us per step, per event pair:
+    // every unit split 199.6, the last 224 / 192 / 160 / 128 / 96 units
+    // split 199.4 / 198.6 / 198.3 / 198.4 / 198.9). LF_SPLIT_TAIL sets how
+    // many of the last units the scoring kernel takes.
+    pl.split_from = 0;
+    if (pl.split) {
+        const long long ctas = static_cast<long long>(units) * pl.nchunk;
+        if (ctas >= 4LL * 3 * sms) pl.split_from = units * 3 / 8;
+        if (const char* env = std::getenv("LF_SPLIT_TAIL"))
+            pl.split_from = std::max(0, units - std::max(1, std::atoi(env)));
+    }
     return pl;
 }
 
@@ -527,6 +544,7 @@ lf_status build_launch(const StepArgs& a, const Shape& s, char* base, uint32_t* 
     sp.topk = a.score ? a.topk : 1;
     sp.flags = a.score ? a.flags : 0;
     sp.split = (a.score && pl.split && sp.topk == 1) ? 1 : 0;
+    sp.split_from = sp.split ? pl.split_from : 0;
     if (!lf::step_fits(s.d, g, pl.stages, a.score, pl.nchunk, sp.topk))
         return fail(LF_ERR_UNSUPPORTED,
                     "k = %d with %d chunks of the slot axis does not fit in shared memory",

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kScoreThreads, G >= 8 ? 4 : 8) lf_score_kernel
     __shared__ unsigned char s_live[kScoreMaxChunks];
     __shared__ unsigned long long s_red[kScoreWarps];
     const int part = blockIdx.x;
-    const int u = blockIdx.y;
+    const int u = p.split_from + static_cast<int>(blockIdx.y);
     const int tid = threadIdx.x;
     if (tid == 0) {
         if (ld_acquire_gpu(p.ready + u) == 0u) {
@@ -176,6 +176,14 @@ __global__ void __launch_bounds__(kScoreThreads, G >= 8 ? 4 : 8) lf_score_kernel
             discard_range(stash + static_cast<size_t>(c) * cs * G,
                           static_cast<size_t>(min(S, (c + 1) * cs) - c * cs) * G * 4, tid,
                           kScoreThreads);
+    // This grid waits for no unit of the decode-step grid that it does not
+    // score, and its other CTAs wait only for flags: the grid's last CTA
+    // also waits for the decode-step grid to complete, so that this grid
+    // completes after it and the next kernel's dependency wait covers both
+    // (the units that scan in their last CTA, and the decode CTAs' last
+    // stores after their flags).
+    if (tid == 0 && blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1)
+        grid_dependency_wait();
 }
 
 template <int D, int G>
@@ -197,7 +205,7 @@ cudaError_t launch_score_t(const StepParams& p, int units, cudaStream_t stream, 
     if (const char* env = std::getenv("LF_SCORE_PARTS")) parts = std::atoi(env);  // tests, tuning
     parts = std::max(1, std::min(p.nchunk, parts));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(parts, units);
+    cfg.gridDim = dim3(parts, units - p.split_from);
     cfg.blockDim = dim3(kScoreThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

@@ -45,6 +45,10 @@ struct StepParams {
     uint32_t* score_arrivals = nullptr;    // [units] arrival counters of the scoring kernel
     uint32_t* ready = nullptr;             // [units] 1 once the unit is merged, 0 between steps
     int split = 0;
+    // With split set, units below this one still scan in their last CTA
+    // (their score terms are still in L2 when they merge); the scoring kernel
+    // takes the units from here on.
+    int split_from = 0;
     int Hq, Hkv, S, W, nchunk, chunk_tiles;
     float scale_log2;            // scale * log2(e)
     int topk;                    // slots returned per unit (1 = the argmin)
@@ -102,8 +106,8 @@ int max_active_clusters(int D, int G, int stages, bool score, int csize);
 // in shared memory (the plan gives that ring no longer chunks).
 int deep_term_slots(int D, int G);
 
-// The scoring kernel of a split finish: grid (parts, units); CTA (c, u)
-// waits for unit u's ready flag, scores its chunks from the ages, the score
+// The scoring kernel of a split finish: grid (parts, units - split_from);
+// CTA (c, y) takes unit u = split_from + y: it waits for unit u's ready flag, scores its chunks from the ages, the score
 // terms and c_h, and the unit's last CTA writes next_slot (and masks it with
 // kFlagMaskEvicted). It does not wait for the decode-step grid as a whole.
 cudaError_t launch_score(int G, const StepParams& p, int units, cudaStream_t stream);

@@ -488,8 +488,8 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int usabl
     // Chunk liveness for the score scan: the chunks' live-tile masks when
     // they were kept (0: no live slot), else from m_c below.
     // (Loaded into a register now, stored after the (m, l) loads are issued.)
-    const uint32_t* ptl =
-        (p.part_tiles && !p.split) ? p.part_tiles + static_cast<size_t>(u) * nchunk : nullptr;
+    const bool kept = p.part_tiles && !(p.split && u >= p.split_from);
+    const uint32_t* ptl = kept ? p.part_tiles + static_cast<size_t>(u) * nchunk : nullptr;
     const uint32_t my_tiles = (kScore && ptl && tid < nchunk) ? __ldcg(&ptl[tid]) : 0u;
 
     // Per head: m = max_c m_c, l = sum_c l_c 2^(m_c - m), weights
@@ -594,7 +594,7 @@ __device__ void finish_unit(const StepParams& p, int u, uint8_t* smem, int usabl
         if (e < G * D) out[e] = __float2bfloat16_rn(o[k]);
     }
     if constexpr (kScore) {
-        if (p.split) {
+        if (p.split && u >= p.split_from) {
             // The scoring kernel that follows scores the chunks in parallel
             // once the unit's flag is up: publish c_h, then release the flag
             // after every write it reads (c_h, and through the arrival
@@ -1496,7 +1496,7 @@ __global__ void __launch_bounds__(kThreads, kStages == 2 ? 3 : (kStages == 3 ? 2
     const uint32_t rest_tiles = live_tiles & ~((1u << nspec) - 1u);  // nspec <= kStages < 32
     const int nlist = nspec + __popc(rest_tiles);  // tiles the ring delivers
     const int cnt = __popc(live_tiles);            // tiles holding a live slot
-    if (kScore && !kCluster && tid == 0 && p.part_tiles && !p.split)
+    if (kScore && !kCluster && tid == 0 && p.part_tiles && !(p.split && u >= p.split_from))
         p.part_tiles[static_cast<size_t>(u) * p.nchunk + chunk] = live_tiles;
 
     if (warp == kConsumerWarps) {

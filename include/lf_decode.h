@@ -53,7 +53,7 @@
  *
  * Environment switches, read at every call (tuning and tests; every setting
  * stays within the same tolerances of the exact result, and LF_SPLIT,
- * LF_SCORE_PARTS, LF_SPEC and LF_PDL change no result bit):
+ * LF_SPLIT_TAIL, LF_SCORE_PARTS, LF_SPEC and LF_PDL change no result bit):
  *   LF_CHUNK_TILES=n   64-slot tiles per chunk of the slot axis (1..32);
  *                      a cluster merge may still re-chunk to its size cap
  *   LF_STAGES=3        three-stage TMA ring (two CTAs per SM) instead of two
@@ -70,6 +70,10 @@
  *                      before loading tiles (no speculative first tiles)
  *   LF_SPLIT=0|1       split finish off / on for every top-1 step without
  *                      clusters (default: units of at least 8192 slots)
+ *   LF_SPLIT_TAIL=n    in a split finish, the scoring kernel takes the last
+ *                      n units and the others scan in their last CTA
+ *                      (default: all units, or the last 5/8 of them when
+ *                      the grid runs at least four waves)
  *   LF_SCORE_PARTS=n   scoring-kernel CTAs per unit in a split finish
  *   LF_WAIT_LIMIT_NS=n limit of the pipeline waits (diagnostic)
  *   LF_HOST_ZEROCOPY=0 lf_decode_step_host stages every host buffer

@@ -1,7 +1,9 @@
 """The split finish: for top-1 steps over long units the decode-step kernel
 stops after the chunk merge and a second kernel scores every chunk in
 parallel (LF_SPLIT=1 forces it on every top-1 step without clusters, =0
-keeps the scan in the last CTA).
+keeps the scan in the last CTA). On grids of many waves the scoring kernel
+takes only the later units, and the first ones still scan in their last CTA
+(LF_SPLIT_TAIL sets how many units the scoring kernel takes).
 
 Both finishes do the same arithmetic in the same order, so they must agree
 bit for bit: output, chosen slot, every score, caches and mask, for every
@@ -171,4 +173,57 @@ def test_split_finish_full_workload_steps(monkeypatch):
     assert all(torch.equal(x, y) for x, y in zip(a[0], b[0]))
     assert all(torch.equal(x, y) for x, y in zip(a[1], b[1]))
     assert torch.equal(a[2], b[2]) and torch.equal(a[3], b[3])
+    assert lf.device_errors() == 0
+
+
+@pytest.mark.parametrize("tail", ["1", "37", "80", "159", "160"])
+@pytest.mark.parametrize("entry,flags", [("scores", 0), ("ex", 3), ("step", 0)])
+def test_hybrid_finish_is_bit_identical(monkeypatch, tail, entry, flags):
+    """A split finish whose scoring kernel takes only the last `tail` units
+    (LF_SPLIT_TAIL; the others scan in their last CTA) gives the same bits as
+    the scan in the last CTA for every unit."""
+    monkeypatch.setenv("LF_CHUNK_TILES", "2")
+    rng = np.random.default_rng(500 + int(tail) + len(entry))
+    case = _pins.rand_case(rng, 20, 32, 8, 64, 1000, p_masked=0.2, max_age=3000, ws_mode="any")
+    case["mask"][3, 2, 300:] = -1      # ragged: chunks without a live slot
+    a = _step(case, 8, 0.125, entry, flags, monkeypatch, "0")
+    monkeypatch.setenv("LF_SPLIT_TAIL", tail)
+    b = _step(case, 8, 0.125, entry, flags, monkeypatch, "1")
+    for key in ("out", "next", "mask", "k", "v"):
+        assert torch.equal(a[key], b[key]), key
+    if entry == "scores":
+        assert torch.equal(a["scores"], b["scores"])
+
+
+def test_default_hybrid_finish_at_full_size(monkeypatch):
+    """The full 16K-slot workload (about nine waves) takes the split finish
+    with its first 3/8 units scanning in their last CTA: the same bits as
+    every unit split and as every unit scanning in its last CTA."""
+    wl = WORKLOADS["long_b32_s16384_ragged"]
+    st = initial_state(wl)
+    inp = {k: to_dev(v) for k, v in step_inputs(wl, 2).items()}
+    ws = to_dev(np.random.default_rng(2).integers(0, wl.S, size=(wl.B, wl.Hkv)).astype(np.int32))
+    units = wl.B * wl.Hkv
+    for k in ("LF_SPLIT_TAIL", "LF_SPLIT"):
+        monkeypatch.delenv(k, raising=False)
+    assert lf.step_plan(wl.B, wl.Hq, wl.Hkv, wl.d, wl.S)["split"]
+    res = {}
+    for name, env in (("default", {}), ("all_split", {"LF_SPLIT_TAIL": str(units)}),
+                      ("no_split", {"LF_SPLIT": "0"})):
+        for k in ("LF_SPLIT_TAIL", "LF_SPLIT"):
+            monkeypatch.delenv(k, raising=False)
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
+        mask = to_dev(st["mask"])
+        k_c, v_c = to_dev(st["k_cache"]), to_dev(st["v_cache"])
+        out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.bfloat16, device="cuda")
+        nxt = torch.empty((wl.B, wl.Hkv), dtype=torch.int32, device="cuda")
+        lf.decode_step(inp["q"], k_c, v_c, mask, inp["new_k"], inp["new_v"], ws, out, nxt,
+                       wl.W, wl.scale)
+        torch.cuda.synchronize()
+        res[name] = (out, nxt, mask)
+        del k_c, v_c
+    for name in ("all_split", "no_split"):
+        for x, y in zip(res["default"], res[name]):
+            assert torch.equal(x, y), name
     assert lf.device_errors() == 0

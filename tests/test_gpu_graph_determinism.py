@@ -27,11 +27,17 @@ def _two_steps(wl, state, inputs, stream, ws0, nxt1, nxt2, out):
                        out, nx, wl.W, wl.scale, stream=stream)
 
 
-@pytest.mark.parametrize("name", ["qwen3_8b_b1_s2400", "llama8b_b256_s2400_ragged",
-                                  "long_b32_s16384_ragged"])
-def test_cuda_graph_replay_equals_eager(name):
+@pytest.mark.parametrize("name,env", [("qwen3_8b_b1_s2400", {}),
+                                      ("llama8b_b256_s2400_ragged", {}),
+                                      ("long_b32_s16384_ragged", {}),
+                                      ("long_b32_s16384_ragged", {"LF_SPLIT_TAIL": "10"})])
+def test_cuda_graph_replay_equals_eager(monkeypatch, name, env):
     """The 16K-slot workload takes the split finish: two kernels per step,
-    both chained by programmatic dependent launch inside the graph."""
+    both chained by programmatic dependent launch inside the graph (with
+    LF_SPLIT_TAIL its first units scan in their last CTA, the scoring
+    kernel takes the last 10)."""
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
     wl = WORKLOADS[name]
     if wl.B > 16:
         wl = wl.with_batch(16 if wl.S <= 4096 else 2)

@@ -79,6 +79,7 @@ def test_prepared_loop_matches_plain_entry(name, io):
 
 @pytest.mark.parametrize("name,batch", [("long_b32_s16384_ragged", 2),      # clusters of 16
                                         ("long_b32_s16384_ragged", 8),      # split finish
+                                        ("long_b32_s16384_ragged", 32),     # split finish, first 3/8 of the units in-kernel
                                         ("llama8b_b256_s2400_ragged", 8),   # clusters
                                         ("qwen3_8b_b128_s3200", 64)])       # last-CTA merge
 def test_prepared_plans(name, batch):

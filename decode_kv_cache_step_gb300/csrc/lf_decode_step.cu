@@ -16,17 +16,19 @@ namespace {
 // kernel, launched behind it with programmatic dependent launch, scores every
 // chunk of every unit in parallel, each unit as soon as its flag is up:
 // log2 I_j from the terms t_hj + c_h, the same arithmetic in the same order
-// as the single-kernel scan, so scores and choices are bit-identical. The lexicographic (I_j, j) argmin is an atomic maximum over
-// the complemented 64-bit key (ordered log2 I_j, slot), empty slots
-// (fill-empty-first) taking score key 0; the last CTA of the unit reads and
-// clears it.
+// as the single-kernel scan, so scores and choices are bit-identical. The
+// lexicographic (I_j, j) argmin is an atomic maximum over the complemented
+// 64-bit key (ordered log2 I_j, slot), empty slots (fill-empty-first) taking
+// score key 0; the last CTA of the unit reads and clears it. Units below
+// split_from (the first ones of a grid of many waves) scan in their last
+// CTA instead, and this grid covers only the others.
 constexpr int kScoreThreads = 128;
 constexpr int kScoreWarps = kScoreThreads / 32;
 constexpr int kScoreTilesPerWarp = 2;  // tiles a warp loads per round trip (4 slots per lane)
 constexpr int kScoreMaxChunks = 1024;
 
-// CTA (part, u) scores the chunks [part * per, (part + 1) * per) of unit u,
-// per = ceil(nchunk / parts) (one chunk by default). Warps take whole
+// CTA (part, y) scores the chunks [part * per, (part + 1) * per) of unit
+// u = split_from + y, per = ceil(nchunk / parts) (one chunk by default). Warps take whole
 // 64-slot tiles, so a tile's chunk and liveness are warp-uniform and a tile
 // of a chunk without a live slot costs no load.
 template <int G>
